@@ -1,0 +1,187 @@
+"""CPU oracle for the SSD forward scan -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA path shares no code with it.
+
+Two independent formulations, both in fp64:
+
+* ``recurrent`` -- the token-by-token selective SSM recurrence, in C
+  (``ssd_oracle.c``, built with gcc/OpenMP by ``build()``).  Source: Mamba-1
+  walkthrough "Mamba: Linear-Time Sequence Modeling with Selective State
+  Spaces", section 三(二) (selective SSM with input-dependent B, C, Delta) and
+  section 三 3 (Abar = exp(Delta A)).
+* ``quadratic`` -- the same linear map written as multiplication by the
+  semiseparable matrix M = L o (C B^T) (QbitAI article "新架构Mamba更新二代！",
+  section "统一SSM和注意力机制": an SSM is a semiseparable-matrix transform and
+  is equivalent to masked attention whose mask L is semiseparable).  It is
+  O(T^2) per (sequence, head) and meant for tiny inputs only.  Every decay
+  sum is formed directly as a sum over its own range, never as a difference
+  of two cumulative sums.
+
+Readings taken where the pages are silent (one A scalar per head, Bbar = dt B,
+y from the updated state, an optional D skip term, contiguous head -> group
+mapping, exact state reset at packed-sequence boundaries) are shared by both
+formulations because both are written from the same definition.
+
+Parity unpinned: nothing.  Every function here is pinned by the tests in
+``tests/test_oracle_pins.py`` against closed forms, hand-computed golden
+fixtures, the recurrent/quadratic duality, and invariants.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssd_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+# Mutations that tests plant in the oracle (see ssd_oracle.c).
+MUTATIONS = {
+    "y_from_old_state": 1,
+    "decay_sign": 2,
+    "group_map": 3,
+    "drop_D": 4,
+    "drop_dt_input": 5,
+    "no_reset": 6,
+}
+
+
+def build(force: bool = False) -> str:
+    """Compile ssd_oracle.c into liboracle.so with gcc (-O2 -fopenmp)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99",
+               "-Wall", "-o", _LIB, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        d = ctypes.c_void_p
+        i64, i32 = ctypes.c_int64, ctypes.c_int
+        lib.ssd_oracle_recurrent.argtypes = [i64, i64, i32, i32, i32, i32, i32,
+                                             d, d, d, d, d, d, d, d, d, d, d, i32, i32]
+        lib.ssd_oracle_recurrent.restype = i32
+        lib.ssd_oracle_recurrent_mut.argtypes = [i64, i64, i32, i32, i32, i32, i32,
+                                                 d, d, d, d, d, d, d, d, d, d, i32]
+        lib.ssd_oracle_recurrent_mut.restype = i32
+        lib.ssd_oracle_max_threads.restype = i32
+        _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    return int(_load().ssd_oracle_max_threads())
+
+
+def _f64(a) -> Optional[np.ndarray]:
+    """Exact upcast of a torch tensor (fp32/bf16) or array to contiguous fp64."""
+    if a is None:
+        return None
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu")
+        import torch
+        a = a.to(torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _prep(x, dt, A, B, C, D, initial_states, cu_seqlens):
+    x, dt, A, B, C = (_f64(t) for t in (x, dt, A, B, C))
+    D = _f64(D)
+    init = _f64(initial_states)
+    cu = None
+    if cu_seqlens is not None:
+        if hasattr(cu_seqlens, "detach"):
+            cu_seqlens = cu_seqlens.detach().cpu().numpy()
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    nseq = (len(cu) - 1) if cu is not None else b
+    return x, dt, A, B, C, D, init, cu, (b, L, H, P, N, G, nseq)
+
+
+def recurrent(x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None,
+              units: Optional[Sequence[int]] = None, nthreads: int = 0,
+              mutation: Optional[str] = None):
+    """fp64 token-by-token recurrence.  Returns (y, final_states) as float64.
+
+    ``units`` restricts the work to the listed (sequence * H + head) units;
+    rows of y belonging to other units are left as NaN.
+    """
+    lib = _load()
+    x, dt, A, B, C, D, init, cu, (b, L, H, P, N, G, nseq) = _prep(
+        x, dt, A, B, C, D, initial_states, cu_seqlens)
+    y = np.full((b, L, H, P), np.nan)
+    fin = np.full((nseq, H, P, N), np.nan)
+    if mutation is not None:
+        rc = lib.ssd_oracle_recurrent_mut(b, L, H, P, N, G, nseq, _ptr(cu), _ptr(x), _ptr(dt),
+                                          _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init),
+                                          _ptr(y), _ptr(fin), MUTATIONS[mutation])
+    else:
+        uarr = None
+        if units is not None:
+            uarr = np.ascontiguousarray(np.asarray(list(units), dtype=np.int32))
+        rc = lib.ssd_oracle_recurrent(b, L, H, P, N, G, nseq, _ptr(cu), _ptr(x), _ptr(dt),
+                                      _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init),
+                                      _ptr(y), _ptr(fin), _ptr(uarr),
+                                      0 if uarr is None else len(uarr), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return y, fin
+
+
+def quadratic(x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None):
+    """fp64 semiseparable-matrix form, y = (L o (C B^T)) . X + init term + D x.
+
+    For each sequence and head, with a_k = dt_k A_h:
+      M[i, j]  = (C_i . B_j) * exp(sum_{k=j+1..i} a_k) * dt_j      (j <= i)
+      y_i      = sum_j M[i, j] x_j + exp(sum_{k<=i} a_k) C_i . S0 + D_h x_i
+      final    = exp(sum_k a_k) S0 + sum_j exp(sum_{k>j} a_k) dt_j x_j (outer) B_j
+    Every exponent is a direct sum over its own index range.
+    """
+    x, dt, A, B, C, D, init, cu, (b, L, H, P, N, G, nseq) = _prep(
+        x, dt, A, B, C, D, initial_states, cu_seqlens)
+    y = np.zeros((b, L, H, P))
+    fin = np.zeros((nseq, H, P, N))
+    hpg = H // G
+    for s in range(nseq):
+        row = 0 if cu is not None else s
+        t0 = int(cu[s]) if cu is not None else 0
+        t1 = int(cu[s + 1]) if cu is not None else L
+        T = t1 - t0
+        for h in range(H):
+            g = h // hpg
+            a = dt[row, t0:t1, h] * A[h]
+            Xs = x[row, t0:t1, h, :]                 # (T, P)
+            Bs = B[row, t0:t1, g, :]                 # (T, N)
+            Cs = C[row, t0:t1, g, :]
+            dts = dt[row, t0:t1, h]
+            M = np.zeros((T, T))
+            for i in range(T):
+                for j in range(i + 1):
+                    M[i, j] = float(Cs[i] @ Bs[j]) * np.exp(np.sum(a[j + 1:i + 1])) * dts[j]
+            yv = M @ Xs
+            S0 = init[s, h] if init is not None else np.zeros((P, N))
+            for i in range(T):
+                yv[i] += np.exp(np.sum(a[:i + 1])) * (S0 @ Cs[i])
+            if D is not None:
+                yv += D[h] * Xs
+            y[row, t0:t1, h, :] = yv
+            F = np.exp(np.sum(a)) * S0
+            for j in range(T):
+                F = F + np.exp(np.sum(a[j + 1:])) * dts[j] * np.outer(Xs[j], Bs[j])
+            fin[s, h] = F
+    return y, fin

@@ -1,0 +1,241 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+* hand-derived golden fixtures (tests/golden/*.json);
+* closed forms: A = 0 gives prefix sums, constant decay gives a geometric
+  series, dt = 0 freezes the state, L = 1;
+* the duality of the recurrent and semiseparable-matrix forms (two separately
+  written formulations of the same map);
+* invariants: splitting a sequence and passing final_states as initial_states
+  reproduces the unsplit run; packed sequences equal separate runs; linearity
+  in (x, initial_states); the unit subset equals the full run;
+* a one-sided check that a huge dt with A < 0 replaces the state by the
+  current input (boundary resetting, Mamba-1 walkthrough section 三 2.3);
+* planted mistakes in the oracle are caught by at least one of these pins.
+"""
+import glob
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ssd_synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand_case(seed, b=1, L=40, H=4, P=3, N=5, G=2, init=True, D=True, cu=None):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(b, L, H, P, generator=g, dtype=torch.float64)
+    dt = torch.rand(b, L, H, generator=g, dtype=torch.float64) * 0.5 + 0.01
+    A = -torch.rand(H, generator=g, dtype=torch.float64) * 3 - 0.1
+    B = torch.randn(b, L, G, N, generator=g, dtype=torch.float64)
+    C = torch.randn(b, L, G, N, generator=g, dtype=torch.float64)
+    Dv = torch.randn(H, generator=g, dtype=torch.float64) if D else None
+    nseq = (len(cu) - 1) if cu is not None else b
+    S0 = torch.randn(nseq, H, P, N, generator=g, dtype=torch.float64) if init else None
+    cuv = None if cu is None else torch.tensor(cu, dtype=torch.int32)
+    return dict(x=x, dt=dt, A=A, B=B, C=C, D=Dv, initial_states=S0, cu_seqlens=cuv)
+
+
+def _golden_cases():
+    return sorted(glob.glob(os.path.join(GOLDEN, "*.json")))
+
+
+@pytest.mark.parametrize("path", _golden_cases(), ids=lambda p: os.path.basename(p))
+@pytest.mark.parametrize("form", ["recurrent", "quadratic"])
+def test_golden_fixture(path, form):
+    with open(path) as f:
+        g = json.load(f)
+    A = np.array(g["A_log2_multiple"]) * math.log(2.0)
+    args = dict(x=np.array(g["x"]), dt=np.array(g["dt"]), A=A, B=np.array(g["B"]),
+                C=np.array(g["C"]), D=np.array(g["D"]),
+                initial_states=None if g["initial_states"] is None else np.array(g["initial_states"]),
+                cu_seqlens=g["cu_seqlens"])
+    y, fin = getattr(oracle, form)(**args)
+    np.testing.assert_allclose(y, np.array(g["y"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(fin, np.array(g["final_states"]), rtol=0, atol=1e-12)
+
+
+def test_prefix_sum_when_A_zero():
+    # A = 0, N = P = 1, B = C = dt = 1, D = 0: the state is the running sum of x.
+    L = 200
+    x = np.random.default_rng(1).standard_normal((1, L, 1, 1))
+    ones = np.ones((1, L, 1, 1))
+    y, fin = oracle.recurrent(x, np.ones((1, L, 1)), np.zeros(1), ones, ones)
+    np.testing.assert_allclose(y[0, :, 0, 0], np.cumsum(x[0, :, 0, 0]), rtol=1e-13, atol=1e-12)
+    assert abs(fin[0, 0, 0, 0] - x.sum()) < 1e-11
+
+
+@pytest.mark.parametrize("dtv,Av", [(0.3, -0.7), (0.05, -4.0), (1.0, -1e-3)])
+def test_geometric_closed_form(dtv, Av):
+    # Constant a = dt A, N = P = 1, B = C = 1, constant x:
+    # y_t = dt x (1 - e^{a (t+1)}) / (1 - e^{a}).
+    L, xv = 300, 1.7
+    a = dtv * Av
+    t = np.arange(L)
+    expect = dtv * xv * (1 - np.exp(a * (t + 1))) / (1 - np.exp(a))
+    y, _ = oracle.recurrent(np.full((1, L, 1, 1), xv), np.full((1, L, 1), dtv), np.array([Av]),
+                            np.ones((1, L, 1, 1)), np.ones((1, L, 1, 1)))
+    np.testing.assert_allclose(y[0, :, 0, 0], expect, rtol=1e-12)
+
+
+def test_dt_zero_freezes_state():
+    c = _rand_case(3)
+    c["dt"] = torch.zeros_like(c["dt"])
+    y, fin = oracle.recurrent(**c)
+    S0 = c["initial_states"].numpy()
+    C, x, D = c["C"].numpy(), c["x"].numpy(), c["D"].numpy()
+    H, G = x.shape[2], C.shape[2]
+    for h in range(H):
+        g = h // (H // G)
+        expect = np.einsum("pn,tn->tp", S0[0, h], C[0, :, g]) + D[h] * x[0, :, h]
+        np.testing.assert_allclose(y[0, :, h], expect, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(fin, S0, rtol=0, atol=0)
+
+
+def test_single_token_closed_form():
+    c = _rand_case(4, L=1)
+    y, fin = oracle.recurrent(**c)
+    x, dt, A, B, C, D, S0 = (c[k].numpy() for k in ("x", "dt", "A", "B", "C", "D", "initial_states"))
+    H, G = x.shape[2], B.shape[2]
+    for h in range(H):
+        g = h // (H // G)
+        S = np.exp(dt[0, 0, h] * A[h]) * S0[0, h] + dt[0, 0, h] * np.outer(x[0, 0, h], B[0, 0, g])
+        np.testing.assert_allclose(fin[0, h], S, rtol=1e-14, atol=1e-14)
+        np.testing.assert_allclose(y[0, 0, h], S @ C[0, 0, g] + D[h] * x[0, 0, h], rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("seed,kw", [
+    (10, dict()),
+    (11, dict(b=2, G=1, init=False)),
+    (12, dict(H=6, G=3, D=False)),
+    (13, dict(cu=[0, 7, 8, 25, 40])),
+    (14, dict(cu=[0, 1, 40], init=False)),
+])
+def test_recurrent_equals_quadratic(seed, kw):
+    c = _rand_case(seed, **kw)
+    y1, f1 = oracle.recurrent(**c)
+    y2, f2 = oracle.quadratic(**c)
+    np.testing.assert_allclose(y1, y2, rtol=1e-11, atol=1e-11 * np.abs(y2).max())
+    np.testing.assert_allclose(f1, f2, rtol=1e-11, atol=1e-11 * np.abs(f2).max())
+
+
+def test_recurrent_equals_quadratic_tiny_fp32_workload():
+    # The whole tiny fp32 workload (L=256, 2 heads, P=N=16) in both forms.
+    inp = ssd_synth.make_inputs(ssd_synth.WORKLOADS[0], seed=0)
+    args = {k: inp[k] for k in ("x", "dt", "A", "B", "C", "D", "initial_states", "cu_seqlens")}
+    y1, f1 = oracle.recurrent(**args)
+    y2, f2 = oracle.quadratic(**args)
+    assert np.abs(y1 - y2).max() <= 1e-12 * np.abs(y2).max()
+    assert np.abs(f1 - f2).max() <= 1e-12 * np.abs(f2).max()
+
+
+@pytest.mark.parametrize("t0", [1, 17, 39])
+def test_split_invariance(t0):
+    c = _rand_case(20, b=1)
+    y, fin = oracle.recurrent(**c)
+    first = {k: (v[:, :t0] if k in ("x", "dt", "B", "C") else v) for k, v in c.items()}
+    y1, f1 = oracle.recurrent(**first)
+    second = {k: (v[:, t0:] if k in ("x", "dt", "B", "C") else v) for k, v in c.items()}
+    second["initial_states"] = f1
+    y2, f2 = oracle.recurrent(**second)
+    np.testing.assert_allclose(np.concatenate([y1, y2], axis=1), y, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(f2, fin, rtol=1e-12, atol=1e-12)
+
+
+def test_packed_equals_separate():
+    cu = [0, 5, 6, 30, 40]
+    c = _rand_case(21, cu=cu)
+    y, fin = oracle.recurrent(**c)
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        sep = {k: (v[:, a:b] if k in ("x", "dt", "B", "C") else v) for k, v in c.items()}
+        sep["cu_seqlens"] = None
+        sep["initial_states"] = c["initial_states"][s:s + 1]
+        ys, fs = oracle.recurrent(**sep)
+        np.testing.assert_allclose(y[:, a:b], ys, rtol=0, atol=0)
+        np.testing.assert_allclose(fin[s:s + 1], fs, rtol=0, atol=0)
+
+
+def test_linearity():
+    c1 = _rand_case(30, D=True)
+    c2 = _rand_case(31, D=True)
+    for k in ("dt", "A", "B", "C", "D"):
+        c2[k] = c1[k]
+    y1, f1 = oracle.recurrent(**c1)
+    y2, f2 = oracle.recurrent(**c2)
+    c3 = dict(c1)
+    c3["x"] = 2.0 * c1["x"] - 3.0 * c2["x"]
+    c3["initial_states"] = 2.0 * c1["initial_states"] - 3.0 * c2["initial_states"]
+    y3, f3 = oracle.recurrent(**c3)
+    np.testing.assert_allclose(y3, 2 * y1 - 3 * y2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(f3, 2 * f1 - 3 * f2, rtol=1e-12, atol=1e-12)
+
+
+def test_huge_dt_replaces_state():
+    # dt -> infinity with A < 0: exp(dt A) -> 0, so the state after token t is
+    # dt_t x_t (outer) B_t regardless of the past (one-sided check).
+    c = _rand_case(40, L=10, D=False)
+    c["dt"] = torch.full_like(c["dt"], 80.0)
+    c["A"] = -torch.ones_like(c["A"])
+    y, fin = oracle.recurrent(**c)
+    x, B, C = c["x"].numpy(), c["B"].numpy(), c["C"].numpy()
+    H, G = x.shape[2], B.shape[2]
+    for h in range(H):
+        g = h // (H // G)
+        S = 80.0 * np.outer(x[0, -1, h], B[0, -1, g])
+        np.testing.assert_allclose(fin[0, h], S, rtol=1e-12, atol=1e-12)
+        for t in range(10):
+            expect = 80.0 * x[0, t, h] * float(B[0, t, g] @ C[0, t, g])
+            np.testing.assert_allclose(y[0, t, h], expect, rtol=1e-12, atol=1e-12)
+
+
+def test_units_subset_matches_full():
+    c = _rand_case(50, b=2, H=4, G=2)
+    y, fin = oracle.recurrent(**c)
+    units = [1, 6]       # (seq 0, head 1) and (seq 1, head 2)
+    ys, fs = oracle.recurrent(**c, units=units)
+    for u in units:
+        s, h = divmod(u, 4)
+        np.testing.assert_array_equal(ys[s, :, h], y[s, :, h])
+        np.testing.assert_array_equal(fs[s, h], fin[s, h])
+    assert np.isnan(ys[0, :, 0]).all()
+
+
+def test_rejects_bad_cu_seqlens():
+    c = _rand_case(60, cu=[0, 10, 40])
+    c["cu_seqlens"] = torch.tensor([0, 10, 39], dtype=torch.int32)
+    with pytest.raises(ValueError):
+        oracle.recurrent(**c)
+
+
+def _pins_pass(mutation):
+    """Run a subset of the pins against a mutated oracle; True if all pass."""
+    ok = True
+    for path in _golden_cases():
+        with open(path) as f:
+            g = json.load(f)
+        A = np.array(g["A_log2_multiple"]) * math.log(2.0)
+        y, fin = oracle.recurrent(np.array(g["x"]), np.array(g["dt"]), A, np.array(g["B"]),
+                                  np.array(g["C"]), np.array(g["D"]),
+                                  None if g["initial_states"] is None else np.array(g["initial_states"]),
+                                  g["cu_seqlens"], mutation=mutation)
+        ok &= bool(np.allclose(y, np.array(g["y"]), rtol=0, atol=1e-12))
+    c = _rand_case(70, cu=[0, 9, 40])
+    y1, _ = oracle.recurrent(**c, mutation=mutation)
+    y2, _ = oracle.quadratic(**c)
+    ok &= bool(np.allclose(y1, y2, rtol=1e-10, atol=1e-10))
+    return ok
+
+
+@pytest.mark.parametrize("mutation", sorted(oracle.MUTATIONS))
+def test_planted_mistakes_are_caught(mutation):
+    assert not _pins_pass(mutation), f"mutation {mutation} slipped through the pins"
+
+
+def test_unmutated_passes_the_same_pins():
+    assert _pins_pass(None)
