@@ -1,0 +1,381 @@
+"""Benchmark of the SSD forward scan on B300: tokens/s, TFLOP/s, fraction of
+roofline, next to the fp64 CPU oracle.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 2] [--algo auto|simt|tc]
+
+A step is one ssd_scan() over the whole workload (default: the 2.7B-shaped
+SSD layer, batch 4 x 8192 tokens, 80 heads, P=64, N=128, chunk 256, bf16),
+inputs resident in HBM.  Under torchrun each rank runs its own full copy of
+the workload (independent problems: weak scaling, no collective on the data
+path); rank 0 prints one JSON line.
+``--impl reference`` times the CPU oracle on the host cores instead (a bounded
+sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import ssd_synth  # noqa: E402
+
+L2_BYTES = 126 * 1024 * 1024
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0,
+                    source="fallback")
+
+
+def workload_cost(inp):
+    """Algorithmic bytes and FLOPs of one scan over ``inp``.
+
+    bytes: x, y, B, C, dt (+ initial/final states, A, D) each moved once.
+    FLOPs (causal count): per token and head (Q+1)P for the masked intra-chunk
+    product and 4NP for the chunk state and the output from the carried state;
+    per token and group (Q+1)N for C B^T.  The dense count is what square
+    tensor-core tiles execute: 2QP + 4NP per token-head and 2QN per token-group.
+    """
+    b, L, H, P, N, G, Q = (inp[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate",
+                                            "ngroups", "chunk"))
+    esz = 2 if inp["dtype"] == "bf16" else 4
+    T = b * L
+    nbytes = 2 * T * H * P * esz + 2 * T * G * N * esz + T * H * 4 + 2 * H * 4
+    nstates = inp["nseq"] * H * P * N * 4
+    if inp["initial_states"] is not None:
+        nbytes += nstates
+    nbytes += nstates  # final_states written
+    causal = T * (H * ((Q + 1) * P + 4 * N * P) + G * (Q + 1) * N)
+    dense = T * (H * (2 * Q * P + 4 * N * P) + G * 2 * Q * N)
+    return nbytes, causal, dense
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML in a thread."""
+
+    REASONS = {
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+        0x100: "display_clock_setting",
+    }
+
+    def __init__(self, index: int):
+        self.samples = []
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:  # NVML missing: report nothing rather than guess
+            self.max_mhz = None
+        self.window = None
+
+    def _run(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+                rs = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append((time.perf_counter(), mhz, rs))
+            except Exception:
+                pass
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self.ok:
+            self.t.join()
+
+    def summary(self, t0, t1):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["nvml_unavailable"]}
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        note = "in_timed_region"
+        if not inside:
+            # the timed region was shorter than the NVML sampling period: use
+            # the samples closest to it
+            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:5]
+            note = "nearest_to_timed_region"
+        mask = 0
+        for s in inside:
+            mask |= s[2]
+        reasons = [n for bit, n in self.REASONS.items() if mask & bit and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(inside), "window": note}
+
+
+def time_oracle_sample(inp, budget_s: float):
+    """Run the CPU oracle on (sequence, head) units of ``inp`` for about
+    ``budget_s`` seconds, one unit per host thread at a time; return
+    (tokens/s equivalent, units, seconds, threads)."""
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    H, nseq = inp["nheads"], inp["nseq"]
+    threads = oracle.max_threads()
+    cu = inp["cu_seqlens"]
+    seq_len = ([int(cu[s + 1] - cu[s]) for s in range(nseq)] if cu is not None
+               else [inp["seqlen"]] * nseq)
+    order = [(s, h) for h in range(H) for s in range(nseq)]
+
+    def one(u):
+        oracle.recurrent_unit(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                              inp["initial_states"], cu, u[0], u[1])
+        return seq_len[u[0]]
+
+    done, tok_heads = 0, 0
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        while time.perf_counter() - t0 < budget_s and done < len(order):
+            batch = order[done:done + threads]
+            tok_heads += sum(pool.map(one, batch))
+            done += len(batch)
+    elapsed = time.perf_counter() - t0
+    return tok_heads / H / elapsed, done, elapsed, threads
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--algo", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the cpu_baseline leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = ssd_synth.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import mamba_ssd_layer_03_b300 as ssd
+
+    inp = ssd_synth.make_inputs(w, seed=rank)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    shape = ssd.make_shape(inp["batch"], inp["seqlen"], inp["nheads"], inp["headdim"],
+                           inp["dstate"], inp["ngroups"], inp["chunk"], inp["nseq"],
+                           d["x"].dtype, args.algo)
+    algo = ssd.resolve_algo(shape)
+    ws = torch.empty(ssd.workspace_size(shape), dtype=torch.uint8, device=dev)
+    y = torch.empty_like(d["x"])
+    fin = torch.empty(inp["nseq"], inp["nheads"], inp["headdim"], inp["dstate"],
+                      dtype=torch.float32, device=dev)
+
+    def step():
+        ssd.ssd_scan(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], inp["chunk"],
+                     d["initial_states"], d["cu_seqlens"], True, args.algo, out=y,
+                     final_out=fin, workspace=ws)
+
+    stream = torch.cuda.current_stream(dev)
+    # Warm-up (also checks the device status word once).
+    for _ in range(max(args.warmup, 1)):
+        step()
+    rc = ssd.load_library().ssd_check_device_status(ssd._ptr(ws), ssd.ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise ssd.SsdError(rc, "warm-up")
+
+    nbytes, causal, dense = workload_cost(inp)
+    peaks = load_peaks()
+
+    sampler = ClockSampler(local)
+    with sampler:
+        time.sleep(0.05)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+        t_host0 = time.perf_counter()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step_ev[i][0].record(stream)
+            step()
+            step_ev[i][1].record(stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        t_host1 = time.perf_counter()
+        if dist:
+            dist.barrier()
+        time.sleep(0.02)
+    total_ms = ev0.elapsed_time(ev1)
+    per_step = [a.elapsed_time(b) for a, b in step_ev]
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens = inp["batch"] * inp["seqlen"]
+    value = tokens * world * args.steps / (total_ms / 1e3)
+    kernel_ms = statistics.mean(per_step)
+    achieved_gbs = nbytes / (kernel_ms / 1e3) / 1e9
+    tflops = causal / (ms_per_step / 1e3) / 1e12
+    t_roof_ms = max(nbytes / (peaks["hbm_gbs"] * 1e9), causal / (peaks["bf16_tflops"] * 1e12)) * 1e3
+
+    # End-to-end through the public API with host buffers: pinned host -> device
+    # copies of the step's inputs, the scan, and the device -> host read of y.
+    e2e = None
+    if rank == 0 or world > 1:
+        host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        in_keys = ("x", "dt", "A", "B", "C", "D", "initial_states", "cu_seqlens")
+        h2d = sum(host[k].numel() * host[k].element_size() for k in in_keys if host[k] is not None)
+        y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        fin_host = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+        d2h = y_host.numel() * y_host.element_size() + fin_host.numel() * fin_host.element_size()
+        dbuf = {k: (torch.empty_like(d[k]) if d[k] is not None else None) for k in in_keys}
+
+        def e2e_step():
+            for k in in_keys:
+                if host[k] is not None:
+                    dbuf[k].copy_(host[k], non_blocking=True)
+            ssd.ssd_scan(dbuf["x"], dbuf["dt"], dbuf["A"], dbuf["B"], dbuf["C"], dbuf["D"],
+                         inp["chunk"], dbuf["initial_states"], dbuf["cu_seqlens"], True,
+                         args.algo, out=y, final_out=fin, workspace=ws)
+            y_host.copy_(y, non_blocking=True)
+            fin_host.copy_(fin, non_blocking=True)
+
+        for _ in range(max(2, min(args.warmup, 3))):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        k_e2e = max(3, min(args.steps, 10))
+        for _ in range(k_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / k_e2e
+        e2e = {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, units, secs, threads = time_oracle_sample(inp, args.cpu_budget)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{units} of {inp['nseq'] * inp['nheads']} (sequence, head) units of "
+                         f"the same workload, full length, fp64 recurrence, {secs:.1f} s; "
+                         f"tokens/s = unit-tokens / nheads / seconds"}
+
+    if rank == 0:
+        clocks = sampler.summary(t_host0, t_host1)
+        out = {
+            "metric": "SSD fwd tokens/s (TFLOP/s and % of roofline alongside) on 1 B300",
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if inp["dtype"] == "bf16" else "f32",
+            "data": "synthetic (seeded, the workload's distributions)",
+            "config": {"workload": w.name, "batch": inp["batch"], "seqlen": inp["seqlen"],
+                       "nheads": inp["nheads"], "headdim": inp["headdim"], "dstate": inp["dstate"],
+                       "ngroups": inp["ngroups"], "chunk": inp["chunk"], "algo": algo,
+                       "parallelism": f"replicas x{world} (independent problems)",
+                       "l2": f"inputs larger than L2: {nbytes / 1e6:.0f} MB streamed per step vs "
+                             f"{L2_BYTES / 2**20:.0f} MiB L2, no flush"},
+            "tflops": tflops, "tflops_dense_equiv": dense / (ms_per_step / 1e3) / 1e12,
+            "roofline_time_ms": t_roof_ms, "frac_of_roofline": t_roof_ms / ms_per_step,
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
+                         "traffic": None, "peak_source": peaks["source"],
+                         "kernel": "whole ssd_scan step (all launches)",
+                         "algorithmic_bytes": nbytes, "kernel_ms": kernel_ms},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": None,
+            "clocks": clocks,
+        }
+        out["gpu_launches"] = launches_per_step(algo, inp) * args.steps
+        print(json.dumps(out))
+    if dist:
+        dist.destroy_process_group()
+
+
+def launches_per_step(algo, inp):
+    """Kernels libssd launches per ssd_scan() (memset of the status word is
+    a copy-engine op, not a kernel)."""
+    varlen = inp["cu_seqlens"] is not None
+    if algo == "simt":
+        return 4 + (2 if varlen else 0)
+    return 1 + (1 if varlen else 0)
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    inp = ssd_synth.make_inputs(w, seed=0)
+    budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        time_oracle_sample(inp, budget)
+    rates, secs_total, units_total = [], 0.0, 0
+    for _ in range(args.steps):
+        rate, units, secs, threads = time_oracle_sample(inp, budget)
+        rates.append(rate)
+        secs_total += secs
+        units_total += units
+    value = statistics.mean(rates)
+    tokens = inp["batch"] * inp["seqlen"]
+    sample = (f"each step: about {budget:.0f} s of (sequence, head) units of the same workload "
+              f"(full length, fp64 recurrence); tokens/s = unit-tokens / nheads / seconds")
+    out = {
+        "impl": "reference", "metric": "SSD fwd tokens/s (TFLOP/s and % of roofline alongside) on 1 B300",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": tokens / value * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": inp["batch"], "seqlen": inp["seqlen"],
+                   "nheads": inp["nheads"], "headdim": inp["headdim"], "dstate": inp["dstate"],
+                   "ngroups": inp["ngroups"], "chunk": inp["chunk"]},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle",
+                         "cores": threads, "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,157 @@
+/*
+ * ssd.h -- C ABI of the SSD (structured state space duality) forward scan
+ * for NVIDIA B300 (sm_103a).
+ *
+ * What it computes.  For every sequence s and head h (B/C group
+ * g = h / (nheads / ngroups)), with a state h_t in R^{headdim x dstate}
+ * starting at initial_states[s, h] (or zero):
+ *
+ *     h_t = exp(dt_t * A_h) * h_{t-1} + dt_t * (x_t (outer) B_t)
+ *     y_t = h_t . C_t + D_h * x_t
+ *
+ * and final_states[s, h] = h after the sequence's last token.
+ *   - The selective SSM (B, C, Delta functions of the input) and its
+ *     recurrence: Mamba-1 walkthrough "Mamba: Linear-Time Sequence Modeling
+ *     with Selective State Spaces", section 三(二) "引入选择机制到 SSM 中";
+ *     Abar = exp(Delta * A): same page, section 三 3.
+ *   - The same map is multiplication by the semiseparable matrix
+ *     M = L o (C B^T); it is evaluated by block decomposition -- masked
+ *     quadratic matmuls inside each chunk of chunk_size tokens plus a
+ *     recurrence over per-chunk states: QbitAI article "新架构Mamba更新二代！",
+ *     sections "统一SSM和注意力机制" (semiseparable matrices, structured masked
+ *     attention, the two equivalent forms) and "Mamba-2：更强学习能力，更快训练推理"
+ *     (block-decomposition matmul algorithm over the GPU memory hierarchy,
+ *     multi-head SSM, variable sequence length).
+ *   - Packed variable-length sequences reset the state at every cu_seqlens
+ *     boundary: same section of the QbitAI article (variable sequence
+ *     length) and the Mamba-1 walkthrough, section 三 2.3 "边界重置".
+ *   dt is taken as given (already positive, e.g. after softplus): the scan
+ *   applies no softplus, bias or clamp.  The chunk size changes only the
+ *   rounding, never the result.
+ *
+ * Layouts.  Row-major, contiguous, no padding:
+ *   x, y            [batch][seqlen][nheads][headdim]   dtype (fp32 or bf16)
+ *   dt              [batch][seqlen][nheads]            fp32
+ *   A, D            [nheads]                           fp32
+ *   B, C            [batch][seqlen][ngroups][dstate]   dtype
+ *   initial_states,
+ *   final_states    [nseq][nheads][headdim][dstate]    fp32
+ *   cu_seqlens      [nseq + 1]                         int32
+ * Without cu_seqlens, sequence s is batch row s and nseq must equal batch.
+ * With cu_seqlens, batch must be 1 and sequence s is tokens
+ * [cu_seqlens[s], cu_seqlens[s+1]) of that row; cu_seqlens[0] == 0,
+ * cu_seqlens[nseq] == seqlen, non-decreasing (an empty sequence's final
+ * state is its initial state).
+ *
+ * Ownership and execution.  Every pointer argument except `shape` and
+ * `bytes` is a DEVICE pointer owned by the caller.  The library allocates
+ * nothing, keeps no state between calls, never synchronises inside
+ * ssd_scan(), and enqueues all its work on `stream` (a cudaStream_t, may be
+ * NULL for the legacy default stream).  Calls on different streams with
+ * different workspaces are independent; the workspace of a call must not be
+ * reused until that call's work on its stream has finished.
+ *
+ * Errors.  Functions return an ssd_status.  Argument errors are detected on
+ * the host before anything is enqueued.  Errors in DEVICE-resident inputs
+ * (a malformed cu_seqlens) and device-side wait time-outs are recorded in
+ * the workspace's status word; the kernels then skip their work and leave
+ * y / final_states unspecified.  ssd_check_device_status() reads that word.
+ * Nothing aborts, traps or throws across this ABI.
+ */
+#ifndef SSD_B300_SSD_H
+#define SSD_B300_SSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSD_API __attribute__((visibility("default")))
+#else
+#define SSD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ssd_dtype {
+    SSD_F32 = 0,   /* x, B, C, y in fp32; all arithmetic fp32 SIMT */
+    SSD_BF16 = 1   /* x, B, C, y in bf16; tensor-core contractions with
+                      fp32 accumulation, fp32 decays and states */
+} ssd_dtype;
+
+typedef enum ssd_algo {
+    SSD_ALGO_AUTO = 0,  /* tensor-core path when the shape allows, else SIMT */
+    SSD_ALGO_SIMT = 1,  /* CUDA-core kernels, any supported shape/dtype */
+    SSD_ALGO_TC = 2     /* tcgen05/TMEM/TMA path (bf16 only); UNSUPPORTED if
+                           the shape does not fit it */
+} ssd_algo;
+
+typedef enum ssd_status {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1,     /* null pointer, bad shape, nseq mismatch */
+    SSD_ERR_UNSUPPORTED = 2,     /* dtype/chunk/headdim/dstate/alignment not
+                                    supported by the requested algorithm */
+    SSD_ERR_WORKSPACE = 3,       /* workspace missing or too small */
+    SSD_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed */
+    SSD_ERR_DEVICE_TIMEOUT = 5,  /* a bounded device-side wait gave up */
+    SSD_ERR_DEVICE_INPUT = 6     /* cu_seqlens (device memory) malformed */
+} ssd_status;
+
+typedef struct ssd_shape {
+    int64_t batch;       /* >= 0 */
+    int64_t seqlen;      /* >= 0, tokens per batch row */
+    int32_t nheads;      /* H >= 1 */
+    int32_t headdim;     /* P, 1..256 (SIMT); 64 (TC) */
+    int32_t dstate;      /* N, 1..256 (SIMT); 64, 128 or 256 (TC) */
+    int32_t ngroups;     /* G >= 1, divides nheads */
+    int32_t chunk_size;  /* Q in {64, 128, 256} */
+    int32_t nseq;        /* number of sequences: batch, or len(cu_seqlens)-1 */
+    int32_t dtype;       /* ssd_dtype */
+    int32_t algo;        /* ssd_algo */
+} ssd_shape;
+
+/*
+ * Bytes of device workspace ssd_scan() needs for `shape` (with the algorithm
+ * the shape resolves to).  Writes *bytes; returns SSD_OK or the same
+ * argument/support error ssd_scan() would return for this shape.
+ */
+SSD_API int ssd_scan_workspace_size(const ssd_shape *shape, size_t *bytes);
+
+/*
+ * Enqueue the SSD forward scan on `stream`.
+ *   x, dt, A, B, C     required inputs (layouts above)
+ *   D                  nullable: treated as all zeros
+ *   initial_states     nullable: zero initial states
+ *   cu_seqlens         nullable: no packing (nseq == batch)
+ *   y                  required output, same dtype as x
+ *   final_states       nullable: not written
+ *   workspace          device buffer of >= ssd_scan_workspace_size() bytes,
+ *                      256-byte aligned; contents need no initialisation
+ * The tensor-core path additionally needs x, B, C, y 16-byte aligned.
+ */
+SSD_API int ssd_scan(const ssd_shape *shape, const void *x, const float *dt,
+                     const float *A, const void *B, const void *C,
+                     const float *D, const float *initial_states,
+                     const int32_t *cu_seqlens, void *y, float *final_states,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronise `stream`, then read the status word that the last ssd_scan()
+ * using `workspace` left there: SSD_OK, SSD_ERR_DEVICE_INPUT or
+ * SSD_ERR_DEVICE_TIMEOUT (or SSD_ERR_CUDA if the sync/copy itself failed).
+ */
+SSD_API int ssd_check_device_status(const void *workspace, void *stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+SSD_API const char *ssd_status_string(int status);
+
+/* Which algorithm ssd_scan() would run for `shape` (SSD_ALGO_SIMT or
+ * SSD_ALGO_TC), or a negative ssd_status if the shape is rejected. */
+SSD_API int ssd_resolve_algo(const ssd_shape *shape);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_B300_SSD_H */

@@ -1,0 +1,208 @@
+"""Python binding of the SSD forward scan library (libssd.so, sm_103a).
+
+Argument marshalling only: tensors are checked for dtype/layout, outputs and
+the workspace are allocated with torch on the current CUDA stream, and the
+C-ABI entry points of include/ssd.h are called through ctypes.  Every step of
+the scan runs in the library's CUDA kernels; there is no CPU fallback, and
+importing this package fails loudly if libssd.so has not been built.
+
+    y, final_states = ssd_scan(x, dt, A, B, C, D=None, chunk_size=256,
+                               initial_states=None, cu_seqlens=None,
+                               return_final_states=True)
+
+computes, for every head h (B/C group g = h // (H // G)),
+h_t = exp(dt_t A_h) h_{t-1} + dt_t x_t (outer) B_t and y_t = h_t C_t + D_h x_t,
+with the state reset at every cu_seqlens boundary.  Shapes: x (b, L, H, P),
+dt (b, L, H) fp32, A (H,) fp32, B/C (b, L, G, N), D (H,) fp32,
+initial/final states (nseq, H, P, N) fp32, cu_seqlens (nseq+1,) int32.
+
+If x lives on the CPU, every input is copied to the current CUDA device
+(pinned host memory makes the copies asynchronous), the scan runs there and
+y / final_states are copied back to the host.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libssd.so")
+
+SSD_F32, SSD_BF16 = 0, 1
+ALGOS = {"auto": 0, "simt": 1, "tc": 2}
+STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED",
+          3: "SSD_ERR_WORKSPACE", 4: "SSD_ERR_CUDA", 5: "SSD_ERR_DEVICE_TIMEOUT",
+          6: "SSD_ERR_DEVICE_INPUT"}
+
+
+class SsdShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64),
+                ("nheads", ctypes.c_int32), ("headdim", ctypes.c_int32),
+                ("dstate", ctypes.c_int32), ("ngroups", ctypes.c_int32),
+                ("chunk_size", ctypes.c_int32), ("nseq", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("algo", ctypes.c_int32)]
+
+
+class SsdError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+_lib = None
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libssd.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libssd.so not found at {LIB_PATH}; build it with "
+                          "`python -m mamba_ssd_layer_03_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    sp = ctypes.POINTER(SsdShape)
+    lib.ssd_scan_workspace_size.argtypes = [sp, ctypes.POINTER(sz)]
+    lib.ssd_scan_workspace_size.restype = ctypes.c_int
+    lib.ssd_scan.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.ssd_scan.restype = ctypes.c_int
+    lib.ssd_check_device_status.argtypes = [vp, vp]
+    lib.ssd_check_device_status.restype = ctypes.c_int
+    lib.ssd_status_string.argtypes = [ctypes.c_int]
+    lib.ssd_status_string.restype = ctypes.c_char_p
+    lib.ssd_resolve_algo.argtypes = [sp]
+    lib.ssd_resolve_algo.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().ssd_status_string(int(code)).decode()
+
+
+def make_shape(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, nseq,
+               dtype: torch.dtype, algo: str = "auto") -> SsdShape:
+    if dtype == torch.float32:
+        d = SSD_F32
+    elif dtype == torch.bfloat16:
+        d = SSD_BF16
+    else:
+        raise TypeError(f"x/B/C dtype must be float32 or bfloat16, got {dtype}")
+    return SsdShape(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, nseq, d,
+                    ALGOS[algo])
+
+
+def workspace_size(shape: SsdShape) -> int:
+    n = ctypes.c_size_t(0)
+    rc = load_library().ssd_scan_workspace_size(ctypes.byref(shape), ctypes.byref(n))
+    if rc != 0:
+        raise SsdError(rc, "ssd_scan_workspace_size")
+    return int(n.value)
+
+
+def resolve_algo(shape: SsdShape) -> str:
+    rc = load_library().ssd_resolve_algo(ctypes.byref(shape))
+    if rc < 0:
+        raise SsdError(-rc, "ssd_resolve_algo")
+    return {1: "simt", 2: "tc"}[rc]
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, dtype, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def ssd_scan(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+             C: torch.Tensor, D: Optional[torch.Tensor] = None, chunk_size: int = 256,
+             initial_states: Optional[torch.Tensor] = None,
+             cu_seqlens: Optional[torch.Tensor] = None, return_final_states: bool = True,
+             algo: str = "auto", out: Optional[torch.Tensor] = None,
+             final_out: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None, check_status: bool = False):
+    """Run the SSD forward scan.  Returns (y, final_states or None).
+
+    ``check_status=True`` synchronises and raises if the device reported a
+    malformed cu_seqlens or a timed-out wait.  ``out``/``final_out``/
+    ``workspace`` let a caller reuse buffers (e.g. inside a timing loop).
+    """
+    if x.device.type == "cpu":
+        return _scan_from_host(x, dt, A, B, C, D, chunk_size, initial_states, cu_seqlens,
+                               return_final_states, algo)
+    lib = load_library()
+    dev = x.device
+    if x.dim() != 4:
+        raise ValueError("x must be (batch, seqlen, nheads, headdim)")
+    b, L, H, P = x.shape
+    if B.dim() != 4:
+        raise ValueError("B must be (batch, seqlen, ngroups, dstate)")
+    G, N = B.shape[2], B.shape[3]
+    _check(x, "x", x.dtype, device=dev)
+    _check(dt, "dt", torch.float32, (b, L, H), dev)
+    _check(A, "A", torch.float32, (H,), dev)
+    _check(B, "B", x.dtype, (b, L, G, N), dev)
+    _check(C, "C", x.dtype, (b, L, G, N), dev)
+    if D is not None:
+        _check(D, "D", torch.float32, (H,), dev)
+    nseq = b
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, device=dev)
+        nseq = cu_seqlens.numel() - 1
+    if initial_states is not None:
+        _check(initial_states, "initial_states", torch.float32, (nseq, H, P, N), dev)
+    shape = make_shape(b, L, H, P, N, G, chunk_size, nseq, x.dtype, algo)
+    nbytes = workspace_size(shape)
+    if workspace is None or workspace.numel() < nbytes:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    y = out if out is not None else torch.empty_like(x)
+    fin = None
+    if return_final_states:
+        fin = final_out if final_out is not None else torch.empty(
+            (nseq, H, P, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    rc = lib.ssd_scan(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                      _ptr(D), _ptr(initial_states), _ptr(cu_seqlens), _ptr(y), _ptr(fin),
+                      _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                      ctypes.c_void_p(stream))
+    if rc != 0:
+        raise SsdError(rc, "ssd_scan")
+    if check_status:
+        rc = lib.ssd_check_device_status(_ptr(workspace), ctypes.c_void_p(stream))
+        if rc != 0:
+            raise SsdError(rc, "ssd_scan (device)")
+    return y, fin
+
+
+def _scan_from_host(x, dt, A, B, C, D, chunk_size, initial_states, cu_seqlens,
+                    return_final_states, algo):
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    def up(t):
+        return None if t is None else t.to(dev, non_blocking=True)
+
+    y, fin = ssd_scan(up(x), up(dt), up(A), up(B), up(C), up(D), chunk_size,
+                      up(initial_states), up(cu_seqlens), return_final_states, algo)
+    pin = x.is_pinned()
+    y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=pin)
+    y_h.copy_(y, non_blocking=pin)
+    fin_h = None
+    if fin is not None:
+        fin_h = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=pin)
+        fin_h.copy_(fin, non_blocking=pin)
+    torch.cuda.current_stream(dev).synchronize()
+    return y_h, fin_h

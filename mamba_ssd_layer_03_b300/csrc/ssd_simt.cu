@@ -1,0 +1,319 @@
+// SIMT (CUDA-core) path of the SSD forward scan.
+//
+// This is the fp32 path (its 1e-5 tolerance rules out tf32 tensor cores) and
+// the generic path for any headdim/dstate up to 256.  It follows the block
+// decomposition of the semiseparable matrix M = L o (C B^T) described in the
+// QbitAI article "新架构Mamba更新二代！" (section "统一SSM和注意力机制" for the
+// semiseparable/masked-attention duality, section
+// "Mamba-2：更强学习能力，更快训练推理" for the block-decomposition algorithm):
+//
+//   K1 chunk cumsum   cs_i = sum of a_k = dt_k A_h over the chunk, restarted
+//                     at every packed-sequence start inside the chunk (fp64)
+//   K2 chunk state    S_c = sum_j exp(cs_last - cs_j) dt_j x_j (outer) B_j over
+//                     the chunk's last sequence piece, from a zero state
+//   K3 state passing  E_c (state entering chunk c's first sequence piece):
+//                     E_{c+1} = exp(cs_last) E'_c + S_c, or the next
+//                     sequence's initial state when one starts at the chunk
+//                     boundary; writes final states that end on a chunk end
+//   K5 sequence final final states of packed sequences ending inside a chunk
+//   K4 chunk output   y_i = sum_{j<=i, same seq} (C_i.B_j) exp(cs_i-cs_j) dt_j x_j
+//                           + exp(cs_i) C_i . E(seq(i)) + D_h x_i
+// Decay exponents are differences of fp64 partial sums so that long chunks
+// of strongly decaying heads keep fp32-level relative accuracy.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ssd_device.cuh"
+#include "ssd_internal.h"
+
+namespace ssd {
+namespace {
+
+struct KArgs {
+    int64_t L;
+    int H, P, N, G, Q, nc, nseq, hpg;
+    bool varlen;
+    const void *x;
+    const float *dt, *A;
+    const void *B, *C;
+    const float *D, *init;
+    const int32_t *cu;
+    void *y;
+    float *final_states;
+    int *status;
+    double *cs;   // [b][H][nc][Q]
+    float *S;     // [b][nc][H][P][N]
+    float *E;     // [b][nc][H][P][N]
+};
+
+__device__ __forceinline__ int64_t cs_index(const KArgs &a, int r, int h, int c) {
+    return (((int64_t)r * a.H + h) * a.nc + c) * a.Q;
+}
+__device__ __forceinline__ int64_t st_index(const KArgs &a, int r, int c, int h) {
+    return (((int64_t)r * a.nc + c) * a.H + h) * (int64_t)a.P * a.N;
+}
+// Sequence containing token t of row r, and that sequence's first token.
+__device__ __forceinline__ int seq_of(const KArgs &a, int r, int64_t t) {
+    return a.varlen ? seg_of(a.cu, a.nseq, t) : r;
+}
+__device__ __forceinline__ int64_t seq_start(const KArgs &a, int s) {
+    return a.varlen ? (int64_t)__ldg(a.cu + s) : 0;
+}
+
+// K1: grid (nc, batch), block 128; one thread per head walks its chunk.
+__global__ void k1_chunk_cumsum(KArgs a) {
+    if (status_bad(a.status)) return;
+    const int c = blockIdx.x, r = blockIdx.y;
+    const int64_t t0 = (int64_t)c * a.Q;
+    const int len = (int)min64(a.Q, a.L - t0);
+    for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
+        const double Ah = (double)__ldg(a.A + h);
+        double run = 0.0;
+        int cur = seq_of(a, r, t0);
+        double *out = a.cs + cs_index(a, r, h, c);
+        for (int i = 0; i < len; ++i) {
+            const int64_t t = t0 + i;
+            if (a.varlen) {
+                int s = seg_of(a.cu, a.nseq, t);
+                if (s != cur) { cur = s; run = 0.0; }
+            }
+            run += (double)__ldg(a.dt + ((int64_t)r * a.L + t) * a.H + h) * Ah;
+            out[i] = run;
+        }
+    }
+}
+
+// K2: grid (nc, batch, H), block 256; threads over (p, n).
+template <typename T>
+__global__ void k2_chunk_state(KArgs a) {
+    if (status_bad(a.status)) return;
+    extern __shared__ float w_smem[];  // [Q] weights exp(cs_last - cs_j) dt_j
+    const int c = blockIdx.x, r = blockIdx.y, h = blockIdx.z;
+    const int g = h / a.hpg;
+    const int64_t t0 = (int64_t)c * a.Q;
+    const int len = (int)min64(a.Q, a.L - t0);
+    const int ls = seq_of(a, r, t0 + len - 1);
+    const int j0 = (int)max64(0, seq_start(a, ls) - t0);
+    const double *cs = a.cs + cs_index(a, r, h, c);
+    const double cl = cs[len - 1];
+    for (int j = threadIdx.x; j < a.Q; j += blockDim.x) {
+        float w = 0.f;
+        if (j >= j0 && j < len)
+            w = (float)exp(cl - cs[j]) * __ldg(a.dt + ((int64_t)r * a.L + t0 + j) * a.H + h);
+        w_smem[j] = w;
+    }
+    __syncthreads();
+    const T *x = (const T *)a.x;
+    const T *B = (const T *)a.B;
+    const int PN = a.P * a.N;
+    float *S = a.S + st_index(a, r, c, h);
+    for (int e = threadIdx.x; e < PN; e += blockDim.x) {
+        const int p = e / a.N, n = e % a.N;
+        float acc = 0.f;
+        for (int j = j0; j < len; ++j) {
+            const int64_t tok = (int64_t)r * a.L + t0 + j;
+            acc += w_smem[j] * ld_as_float(x + (tok * a.H + h) * a.P + p) *
+                   ld_as_float(B + (tok * a.G + g) * a.N + n);
+        }
+        S[e] = acc;
+    }
+}
+
+// K3: grid (ceil(P*N/256), H, batch), block 256; one thread per state
+// element walks the chunks of its row in order.
+__global__ void k3_state_passing(KArgs a) {
+    if (status_bad(a.status)) return;
+    const int h = blockIdx.y, r = blockIdx.z;
+    const int PN = a.P * a.N;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= PN) return;
+    float end_state = 0.f;
+    for (int c = 0; c < a.nc; ++c) {
+        const int64_t t0 = (int64_t)c * a.Q;
+        const int len = (int)min64(a.Q, a.L - t0);
+        const int fs = seq_of(a, r, t0);
+        const int ls = seq_of(a, r, t0 + len - 1);
+        float E;
+        if (c == 0 || seq_start(a, fs) == t0)   // a sequence starts here
+            E = a.init ? a.init[((int64_t)fs * a.H + h) * PN + e] : 0.f;
+        else
+            E = end_state;                      // carried across the boundary
+        a.E[st_index(a, r, c, h) + e] = E;
+        float El = (ls == fs) ? E : (a.init ? a.init[((int64_t)ls * a.H + h) * PN + e] : 0.f);
+        const double cl = a.cs[cs_index(a, r, h, c) + len - 1];
+        end_state = (float)exp(cl) * El + a.S[st_index(a, r, c, h) + e];
+        const int64_t t_end = t0 + len - 1;
+        const int64_t seq_last = a.varlen ? (int64_t)__ldg(a.cu + ls + 1) - 1 : a.L - 1;
+        if (a.final_states && seq_last == t_end)
+            a.final_states[((int64_t)ls * a.H + h) * PN + e] = end_state;
+    }
+}
+
+// K5: final states of packed sequences that end inside a chunk (or are
+// empty).  grid (nseq, H), block 256; threads over (p, n).
+template <typename T>
+__global__ void k5_seq_final(KArgs a) {
+    if (status_bad(a.status)) return;
+    extern __shared__ float w_smem[];
+    const int s = blockIdx.x, h = blockIdx.y, g = h / a.hpg;
+    const int PN = a.P * a.N;
+    const int64_t sa = __ldg(a.cu + s), sb = __ldg(a.cu + s + 1);
+    float *fin = a.final_states + ((int64_t)s * a.H + h) * PN;
+    if (sb <= sa) {   // empty sequence: final = initial
+        for (int e = threadIdx.x; e < PN; e += blockDim.x)
+            fin[e] = a.init ? a.init[((int64_t)s * a.H + h) * PN + e] : 0.f;
+        return;
+    }
+    const int64_t T_last = min64(sb - 1, a.L - 1);
+    if (T_last < 0) return;
+    const int c = (int)(T_last / a.Q);
+    const int64_t t0 = (int64_t)c * a.Q;
+    const int len = (int)min64(a.Q, a.L - t0);
+    if (T_last == t0 + len - 1) return;       // ends on a chunk end: K3 wrote it
+    const int fs = seg_of(a.cu, a.nseq, t0);
+    const int iT = (int)(T_last - t0);
+    const int j0 = (int)max64(0, sa - t0);
+    const double *cs = a.cs + cs_index(a, 0, h, c);
+    const double cT = cs[iT];
+    for (int j = threadIdx.x; j < a.Q; j += blockDim.x) {
+        float w = 0.f;
+        if (j >= j0 && j <= iT)
+            w = (float)exp(cT - cs[j]) * __ldg(a.dt + (t0 + j) * a.H + h);
+        w_smem[j] = w;
+    }
+    __syncthreads();
+    const float dec = (float)exp(cT);
+    const float *E = (s == fs) ? a.E + st_index(a, 0, c, h)
+                               : (a.init ? a.init + ((int64_t)s * a.H + h) * PN : nullptr);
+    const T *x = (const T *)a.x;
+    const T *B = (const T *)a.B;
+    for (int e = threadIdx.x; e < PN; e += blockDim.x) {
+        const int p = e / a.N, n = e % a.N;
+        float acc = E ? dec * E[e] : 0.f;
+        for (int j = j0; j <= iT; ++j) {
+            const int64_t tok = t0 + j;
+            acc += w_smem[j] * ld_as_float(x + (tok * a.H + h) * a.P + p) *
+                   ld_as_float(B + (tok * a.G + g) * a.N + n);
+        }
+        fin[e] = acc;
+    }
+}
+
+constexpr int kPT = 16;  // output columns (p) per thread in K4
+
+// K4: grid (nc, batch, H * ceil(P/16)), block Q; thread i owns token i of
+// the chunk and 16 consecutive p columns.
+template <typename T>
+__global__ void k4_chunk_output(KArgs a) {
+    if (status_bad(a.status)) return;
+    const int c = blockIdx.x, r = blockIdx.y;
+    const int npt = (a.P + kPT - 1) / kPT;
+    const int h = blockIdx.z / npt, p0 = (blockIdx.z % npt) * kPT;
+    const int g = h / a.hpg;
+    const int64_t t0 = (int64_t)c * a.Q;
+    const int len = (int)min64(a.Q, a.L - t0);
+    const int i = threadIdx.x;
+    if (i >= len) return;
+    const int64_t ti = t0 + i;
+    const int64_t tok_i = (int64_t)r * a.L + ti;
+    const int si = seq_of(a, r, ti);
+    const int fs = seq_of(a, r, t0);
+    const int j0 = (int)max64(0, seq_start(a, si) - t0);
+    const double *cs = a.cs + cs_index(a, r, h, c);
+    const double csi = cs[i];
+    const T *x = (const T *)a.x;
+    const T *B = (const T *)a.B;
+    const T *C = (const T *)a.C;
+    const T *Ci = C + (tok_i * a.G + g) * a.N;
+    float acc[kPT];
+#pragma unroll
+    for (int q = 0; q < kPT; ++q) acc[q] = 0.f;
+    for (int j = j0; j <= i; ++j) {
+        const int64_t tok_j = (int64_t)r * a.L + t0 + j;
+        const T *Bj = B + (tok_j * a.G + g) * a.N;
+        float cb = 0.f;
+        for (int n = 0; n < a.N; ++n) cb += ld_as_float(Ci + n) * ld_as_float(Bj + n);
+        const float w = cb * expf((float)(csi - cs[j])) * __ldg(a.dt + tok_j * a.H + h);
+        const T *xj = x + (tok_j * a.H + h) * a.P;
+#pragma unroll
+        for (int q = 0; q < kPT; ++q)
+            if (p0 + q < a.P) acc[q] += w * ld_as_float(xj + p0 + q);
+    }
+    const int PN = a.P * a.N;
+    const float *E = (si == fs) ? a.E + st_index(a, r, c, h)
+                                : (a.init ? a.init + ((int64_t)si * a.H + h) * PN : nullptr);
+    if (E) {
+        const float dec = expf((float)csi);
+#pragma unroll
+        for (int q = 0; q < kPT; ++q) {
+            if (p0 + q >= a.P) continue;
+            const float *Ep = E + (int64_t)(p0 + q) * a.N;
+            float s = 0.f;
+            for (int n = 0; n < a.N; ++n) s += ld_as_float(Ci + n) * Ep[n];
+            acc[q] += dec * s;
+        }
+    }
+    const float Dh = a.D ? __ldg(a.D + h) : 0.f;
+    const T *xi = x + (tok_i * a.H + h) * a.P;
+    T *y = (T *)a.y + (tok_i * a.H + h) * a.P;
+#pragma unroll
+    for (int q = 0; q < kPT; ++q)
+        if (p0 + q < a.P) st_from_float(y + p0 + q, acc[q] + Dh * ld_as_float(xi + p0 + q));
+}
+
+struct WsLayout {
+    size_t cs, S, E, total;
+};
+
+WsLayout layout(const Problem &p) {
+    WsLayout w{};
+    const size_t units = (size_t)p.batch * p.nc * p.H;
+    size_t off = 0;
+    w.cs = off; off = align_up(off + units * p.Q * sizeof(double), 256);
+    w.S = off;  off = align_up(off + units * (size_t)p.P * p.N * sizeof(float), 256);
+    w.E = off;  off = align_up(off + units * (size_t)p.P * p.N * sizeof(float), 256);
+    w.total = off;
+    return w;
+}
+
+template <typename T>
+cudaError_t launch_all(const Problem &p) {
+    const WsLayout w = layout(p);
+    KArgs a;
+    a.L = p.seqlen; a.H = p.H; a.P = p.P; a.N = p.N; a.G = p.G; a.Q = p.Q;
+    a.nc = p.nc; a.nseq = p.nseq; a.hpg = p.H / p.G; a.varlen = p.cu != nullptr;
+    a.x = p.x; a.dt = p.dt; a.A = p.A; a.B = p.B; a.C = p.C; a.D = p.D;
+    a.init = p.init; a.cu = p.cu; a.y = p.y; a.final_states = p.final_states;
+    a.status = p.status;
+    a.cs = (double *)(p.ws + w.cs);
+    a.S = (float *)(p.ws + w.S);
+    a.E = (float *)(p.ws + w.E);
+    const unsigned b = (unsigned)p.batch;
+    k1_chunk_cumsum<<<dim3(p.nc, b), 128, 0, p.stream>>>(a);
+    k2_chunk_state<T><<<dim3(p.nc, b, p.H), 256, p.Q * sizeof(float), p.stream>>>(a);
+    const int PN = p.P * p.N;
+    k3_state_passing<<<dim3((PN + 255) / 256, p.H, b), 256, 0, p.stream>>>(a);
+    if (a.varlen && p.final_states)
+        k5_seq_final<T><<<dim3(p.nseq, p.H), 256, p.Q * sizeof(float), p.stream>>>(a);
+    const int npt = (p.P + kPT - 1) / kPT;
+    k4_chunk_output<T><<<dim3(p.nc, b, p.H * npt), p.Q, 0, p.stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t simt_workspace_bytes(const Problem &p) { return layout(p).total; }
+
+int simt_supported(const Problem &p) {
+    if (p.P < 1 || p.P > 256 || p.N < 1 || p.N > 256) return SSD_ERR_UNSUPPORTED;
+    if (p.Q != 64 && p.Q != 128 && p.Q != 256) return SSD_ERR_UNSUPPORTED;
+    if (p.dtype != SSD_F32 && p.dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
+    return SSD_OK;
+}
+
+cudaError_t simt_launch(const Problem &p) {
+    if (p.dtype == SSD_F32) return launch_all<float>(p);
+    return launch_all<__nv_bfloat16>(p);
+}
+
+}  // namespace ssd

@@ -143,6 +143,23 @@ def recurrent(x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None,
     return y, fin
 
 
+def recurrent_unit(x, dt, A, B, C, D, initial_states, cu_seqlens, s: int, h: int):
+    """fp64 recurrence of the single (sequence s, head h) unit, from sliced
+    inputs (only that unit's tokens, head and group are converted to fp64).
+    Returns (y (T, P), final_state (P, N))."""
+    H, G = x.shape[2], B.shape[2]
+    g = h // (H // G)
+    if cu_seqlens is not None:
+        row, t0, t1 = 0, int(cu_seqlens[s]), int(cu_seqlens[s + 1])
+    else:
+        row, t0, t1 = s, 0, x.shape[1]
+    sl = lambda t, k: t[row:row + 1, t0:t1, k:k + 1]
+    S0 = None if initial_states is None else initial_states[s:s + 1, h:h + 1]
+    y, fin = recurrent(sl(x, h), dt[row:row + 1, t0:t1, h:h + 1], A[h:h + 1], sl(B, g), sl(C, g),
+                       None if D is None else D[h:h + 1], S0, None, nthreads=1)
+    return y[0, :, 0, :], fin[0, 0]
+
+
 def quadratic(x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None):
     """fp64 semiseparable-matrix form, y = (L o (C B^T)) . X + init term + D x.
 

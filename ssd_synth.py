@@ -120,8 +120,8 @@ def make_inputs(w: Workload, seed: int = 0, *, batch: Optional[int] = None,
             segs[-1] -= total - L
         else:
             segs = list(segment_lengths)
-            if sum(segs) != L or min(segs) < 1:
-                raise ValueError("segment lengths must be >= 1 and sum to seqlen")
+            if sum(segs) != L or min(segs) < 0:
+                raise ValueError("segment lengths must be >= 0 and sum to seqlen")
         cu = torch.zeros(len(segs) + 1, dtype=torch.int32)
         cu[1:] = torch.cumsum(torch.tensor(segs, dtype=torch.int64), 0).to(torch.int32)
         nseq = len(segs)

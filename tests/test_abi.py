@@ -1,0 +1,113 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+declared in include/ssd.h, sizes workspaces, and rejects bad arguments on the
+host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mamba_ssd_layer_03_b300 as ssd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            with open(os.path.join(ROOT, "include", fn)) as f:
+                text = f.read()
+            names += re.findall(r"SSD_API\s+[\w\s\*]+?\b(ssd_\w+)\s*\(", text)
+    return names
+
+
+def test_header_declares_entry_points():
+    names = _declared_symbols()
+    for n in ("ssd_scan", "ssd_scan_workspace_size", "ssd_check_device_status",
+              "ssd_status_string", "ssd_resolve_algo"):
+        assert n in names
+
+
+@pytest.mark.parametrize("name", _declared_symbols())
+def test_library_exports_declared_symbol(name):
+    lib = ssd.load_library()
+    assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_only_declared_symbols_exported():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", ssd.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    ours = {n for n in exported if n.startswith("ssd_")}
+    assert ours == set(_declared_symbols())
+
+
+def test_status_strings():
+    for code in range(7):
+        s = ssd.status_string(code)
+        assert s.startswith("SSD_")
+    assert ssd.status_string(99) == "SSD_ERR_UNKNOWN"
+
+
+def _shape(**kw):
+    import torch
+    d = dict(batch=4, seqlen=8192, nheads=80, headdim=64, dstate=128, ngroups=1,
+             chunk_size=256, nseq=4, dtype=torch.bfloat16, algo="auto")
+    d.update(kw)
+    return ssd.make_shape(d["batch"], d["seqlen"], d["nheads"], d["headdim"], d["dstate"],
+                          d["ngroups"], d["chunk_size"], d["nseq"], d["dtype"], d["algo"])
+
+
+def test_workspace_size_simt_scales_with_chunks():
+    a = ssd.workspace_size(_shape(algo="simt"))
+    b = ssd.workspace_size(_shape(algo="simt", seqlen=16384))
+    assert a > 0 and b > a
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(chunk_size=100), 2),
+    (dict(chunk_size=32), 2),
+    (dict(ngroups=3), 1),
+    (dict(nheads=0), 1),
+    (dict(headdim=300, algo="simt"), 2),
+    (dict(dstate=512, algo="simt"), 2),
+    (dict(seqlen=-1), 1),
+])
+def test_workspace_size_rejects(kw, code):
+    with pytest.raises(ssd.SsdError) as ei:
+        ssd.workspace_size(_shape(**kw))
+    assert ei.value.code == code
+
+
+def test_scan_rejects_on_host_before_device_work():
+    lib = ssd.load_library()
+    sh = _shape(algo="simt")
+    nbytes = ssd.workspace_size(sh)
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: validation fails first
+    args = [fake] * 5 + [None, None, None, fake, None]
+    # workspace missing
+    assert lib.ssd_scan(ctypes.byref(sh), *args, None, ctypes.c_size_t(0), None) == 3
+    # workspace too small
+    assert lib.ssd_scan(ctypes.byref(sh), *args, fake, ctypes.c_size_t(nbytes - 1), None) == 3
+    # nseq != batch without cu_seqlens
+    bad = _shape(algo="simt", nseq=3)
+    assert lib.ssd_scan(ctypes.byref(bad), *args, fake, ctypes.c_size_t(nbytes), None) == 1
+    # null x with tokens present
+    args2 = [None] + [fake] * 4 + [None, None, None, fake, None]
+    assert lib.ssd_scan(ctypes.byref(sh), *args2, fake, ctypes.c_size_t(nbytes), None) == 1
+    # misaligned bf16 pointer
+    odd = ctypes.c_void_p((1 << 20) + 1)
+    args3 = [odd] + [fake] * 4 + [None, None, None, fake, None]
+    assert lib.ssd_scan(ctypes.byref(sh), *args3, fake, ctypes.c_size_t(nbytes), None) == 2
+    # null shape
+    assert lib.ssd_scan(None, *args, fake, ctypes.c_size_t(nbytes), None) == 1
+    # varlen needs batch == 1
+    cu = fake
+    args4 = [fake] * 5 + [None, None, cu, fake, None]
+    assert lib.ssd_scan(ctypes.byref(sh), *args4, fake, ctypes.c_size_t(nbytes), None) == 1
+
+
+def test_check_status_rejects_null():
+    assert ssd.load_library().ssd_check_device_status(None, None) == 1

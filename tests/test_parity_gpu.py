@@ -1,0 +1,214 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on
+identical seeded inputs.  Bar: max-abs error / max-abs oracle value <= 1e-5
+for fp32 inputs and <= 2e-2 for bf16 inputs, on y and on final_states."""
+import numpy as np
+import pytest
+import torch
+
+import ssd_synth
+from parity_util import (TOL, oracle_full, oracle_unit, rel_err, run_gpu, sample_units,
+                         unit_slices)
+
+pytestmark = pytest.mark.gpu
+
+W = ssd_synth.WORKLOADS
+ALGOS = ["simt"]
+
+
+def _algo_ok(inp, algo):
+    import mamba_ssd_layer_03_b300 as ssd
+    if algo == "simt" or inp["dtype"] == "bf16":
+        return True
+    return False   # the tensor-core path is bf16 only
+
+
+def _compare_full(inp, algo, chunk=None, D=True, init=True):
+    tol = TOL[inp["dtype"]]
+    y, fin = run_gpu(inp, chunk=chunk, algo=algo, D=D, init=init)
+    y_ref, fin_ref = oracle_full(inp, D=D, init=init)
+    ey, ef = rel_err(y, y_ref), rel_err(fin, fin_ref)
+    assert ey <= tol, f"y rel err {ey:.3e} > {tol}"
+    assert ef <= tol, f"final_states rel err {ef:.3e} > {tol}"
+    return ey, ef
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_tiny_fp32_workload_full(algo):
+    inp = ssd_synth.make_inputs(W[0], seed=0)
+    if not _algo_ok(inp, algo):
+        pytest.skip("tensor-core path is bf16 only")
+    _compare_full(inp, algo)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+def test_chunk_size_independence_fp32(algo, chunk):
+    inp = ssd_synth.make_inputs(W[0], seed=1, seqlen=300, init_states=True)
+    if not _algo_ok(inp, algo):
+        pytest.skip("tensor-core path is bf16 only")
+    _compare_full(inp, algo, chunk=chunk)
+
+
+# Reduced-length versions of the bf16 workloads: several chunks plus a ragged
+# tail, small enough for the whole oracle.
+REDUCED = [
+    (1, dict(batch=2, seqlen=1000, nheads=6)),
+    (2, dict(batch=2, seqlen=777, nheads=5)),
+    (3, dict(batch=2, seqlen=1100, nheads=8)),
+    (4, dict(batch=1, seqlen=2000, nheads=4, segment_lengths=[1, 255, 256, 300, 64, 1, 1123])),
+]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("wi,kw", REDUCED, ids=[f"w{w}" for w, _ in REDUCED])
+def test_reduced_workloads_full(algo, wi, kw):
+    inp = ssd_synth.make_inputs(W[wi], seed=wi, **kw)
+    _compare_full(inp, algo)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+def test_chunk_size_independence_bf16(algo, chunk):
+    inp = ssd_synth.make_inputs(W[3], seed=5, batch=1, seqlen=700, nheads=8)
+    _compare_full(inp, algo, chunk=chunk)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("L", [1, 63, 64, 65, 256, 257])
+def test_short_and_boundary_lengths(algo, L):
+    inp = ssd_synth.make_inputs(W[1], seed=L, batch=2, seqlen=L, nheads=3, init_states=True)
+    _compare_full(inp, algo, chunk=64)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_optional_arguments_absent(algo):
+    inp = ssd_synth.make_inputs(W[1], seed=9, batch=1, seqlen=513, nheads=4, init_states=True)
+    y, fin = run_gpu(inp, algo=algo, D=False, init=False, final=False)
+    assert fin is None
+    y_ref, _ = oracle_full(inp, D=False, init=False)
+    assert rel_err(y, y_ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("segs", [
+    [64, 64, 64, 64],            # boundaries exactly on chunk ends
+    [1] * 70,                    # many single-token sequences
+    [100, 0, 0, 156, 0],         # empty sequences
+    [1000],                      # one sequence across many chunks
+    [5, 250, 7, 500, 2, 260],    # mixed
+])
+def test_varlen_edges_with_initial_states(algo, segs):
+    L = sum(segs)
+    inp = ssd_synth.make_inputs(W[4], seed=len(segs), seqlen=L, nheads=3,
+                                init_states=True, segment_lengths=segs)
+    _compare_full(inp, algo, chunk=64)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_varlen_packed_equals_separate_runs(algo):
+    segs = [300, 17, 451]
+    inp = ssd_synth.make_inputs(W[4], seed=77, seqlen=sum(segs), nheads=4,
+                                init_states=True, segment_lengths=segs)
+    y, fin = run_gpu(inp, algo=algo)
+    cu = inp["cu_seqlens"]
+    for s in range(len(segs)):
+        a, b = int(cu[s]), int(cu[s + 1])
+        sep = dict(inp)
+        for k in ("x", "dt", "B", "C"):
+            sep[k] = inp[k][:, a:b].contiguous()
+        sep["cu_seqlens"] = None
+        sep["initial_states"] = inp["initial_states"][s:s + 1].contiguous()
+        sep["seqlen"], sep["nseq"] = b - a, 1
+        ys, fs = run_gpu(sep, algo=algo)
+        assert rel_err(y[:, a:b], ys) <= 1e-2
+        assert rel_err(fin[s:s + 1], fs) <= 1e-2
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_split_invariance_through_states(algo):
+    inp = ssd_synth.make_inputs(W[3], seed=11, batch=2, seqlen=900, nheads=8)
+    y, fin = run_gpu(inp, algo=algo)
+    t0 = 384
+    first, second = dict(inp), dict(inp)
+    for k in ("x", "dt", "B", "C"):
+        first[k] = inp[k][:, :t0].contiguous()
+        second[k] = inp[k][:, t0:].contiguous()
+    first["seqlen"], second["seqlen"] = t0, 900 - t0
+    y1, f1 = run_gpu(first, algo=algo)
+    second["initial_states"] = torch.from_numpy(f1)
+    y2, f2 = run_gpu(second, algo=algo)
+    assert rel_err(np.concatenate([y1, y2], axis=1), y) <= 1e-2
+    assert rel_err(f2, fin) <= 1e-2
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_dt_zero_freezes_state(algo):
+    inp = ssd_synth.make_inputs(W[1], seed=3, batch=1, seqlen=300, nheads=2, init_states=True)
+    inp["dt"] = torch.zeros_like(inp["dt"])
+    y, fin = run_gpu(inp, algo=algo)
+    assert np.array_equal(fin, inp["initial_states"].numpy())
+    _compare_full(inp, algo)
+
+
+# ---- full-size workloads, in the launch configuration the benchmark times ----
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("wi", [1, 2, 3, 4])
+def test_full_size_workload_sampled(algo, wi):
+    inp = ssd_synth.make_inputs(W[wi], seed=0)
+    tol = TOL[inp["dtype"]]
+    y, fin = run_gpu(inp, algo=algo)
+    assert np.isfinite(y).all()
+    for (s, h) in sample_units(inp, 6, seed=wi):
+        yu, fu = oracle_unit(inp, s, h)
+        row, t0, t1, _ = unit_slices(inp, s, h)
+        assert rel_err(y[row, t0:t1, h], yu) <= tol, (s, h)
+        assert rel_err(fin[s, h], fu) <= tol, (s, h)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_full_size_workload1_complete(algo):
+    inp = ssd_synth.make_inputs(W[1], seed=0)
+    _compare_full(inp, algo)
+
+
+def test_malformed_cu_seqlens_reports_status():
+    import mamba_ssd_layer_03_b300 as ssd
+    inp = ssd_synth.make_inputs(W[4], seed=1, seqlen=300, nheads=2, segment_lengths=[100, 200])
+    bad = torch.tensor([0, 200, 100, 300], dtype=torch.int32)  # decreasing
+    dev = "cuda"
+    S0 = torch.zeros(3, 2, 64, 128, device=dev)
+    with pytest.raises(ssd.SsdError) as ei:
+        ssd.ssd_scan(inp["x"].to(dev), inp["dt"].to(dev), inp["A"].to(dev), inp["B"].to(dev),
+                     inp["C"].to(dev), None, 64, S0, bad.to(dev), check_status=True)
+    assert ei.value.code == 6
+    # the context is still usable
+    y, _ = run_gpu(inp)
+    assert np.isfinite(y).all()
+
+
+def test_empty_inputs():
+    import mamba_ssd_layer_03_b300 as ssd
+    dev = "cuda"
+    for b, L in [(2, 0), (0, 16)]:
+        x = torch.zeros(b, L, 2, 64, dtype=torch.bfloat16, device=dev)
+        dt = torch.zeros(b, L, 2, device=dev)
+        A = -torch.ones(2, device=dev)
+        B = torch.zeros(b, L, 1, 128, dtype=torch.bfloat16, device=dev)
+        S0 = torch.randn(b, 2, 64, 128, device=dev)
+        y, fin = ssd.ssd_scan(x, dt, A, B, B.clone(), None, 256, S0 if b else None,
+                              check_status=True)
+        assert y.shape == x.shape
+        if b:
+            assert torch.equal(fin, S0)
+
+
+def test_host_buffers_round_trip():
+    import mamba_ssd_layer_03_b300 as ssd
+    inp = ssd_synth.make_inputs(W[1], seed=4, batch=1, seqlen=600, nheads=3)
+    pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y, fin = ssd.ssd_scan(pin["x"], pin["dt"], pin["A"], pin["B"], pin["C"], pin["D"], 256)
+    assert y.device.type == "cpu" and fin.device.type == "cpu"
+    y_ref, f_ref = oracle_full(inp)
+    assert rel_err(y.float().numpy(), y_ref) <= TOL["bf16"]
+    assert rel_err(fin.numpy(), f_ref) <= TOL["bf16"]
