@@ -119,7 +119,8 @@ SSD_API int ssd_scan(const ssd_shape *shape, const void *x, const float *dt, con
         !aligned(final_states, 4) || !aligned(cu_seqlens, 4))
         return SSD_ERR_UNSUPPORTED;
     if (algo == SSD_ALGO_TC &&
-        (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16)))
+        (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
+         !aligned(initial_states, 16) || !aligned(final_states, 16)))
         return SSD_ERR_UNSUPPORTED;
 
     p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D;

@@ -12,17 +12,31 @@ from parity_util import (TOL, oracle_full, oracle_unit, rel_err, run_gpu, sample
 pytestmark = pytest.mark.gpu
 
 W = ssd_synth.WORKLOADS
-ALGOS = ["simt"]
+ALGOS = ["simt", "tc"]
 
 
-def _algo_ok(inp, algo):
-    import mamba_ssd_layer_03_b300 as ssd
-    if algo == "simt" or inp["dtype"] == "bf16":
+def _algo_ok(inp, algo, chunk=None):
+    """Whether `algo` takes this input (the tensor-core path is bf16 only,
+    headdim 64, dstate 128/256, chunk 128/256, no packed sequences)."""
+    if algo == "simt":
         return True
-    return False   # the tensor-core path is bf16 only
+    import mamba_ssd_layer_03_b300 as ssd
+    dt = torch.float32 if inp["dtype"] == "fp32" else torch.bfloat16
+    shape = ssd.make_shape(inp["batch"], inp["seqlen"], inp["nheads"], inp["headdim"],
+                           inp["dstate"], inp["ngroups"], chunk or inp["chunk"], inp["nseq"], dt,
+                           algo)
+    try:
+        ssd.workspace_size(shape)
+    except ssd.SsdError as e:
+        if e.code == 2:
+            return False
+        raise
+    return inp["cu_seqlens"] is None
 
 
 def _compare_full(inp, algo, chunk=None, D=True, init=True):
+    if not _algo_ok(inp, algo, chunk):
+        pytest.skip(f"{algo} path does not take this input")
     tol = TOL[inp["dtype"]]
     y, fin = run_gpu(inp, chunk=chunk, algo=algo, D=D, init=init)
     y_ref, fin_ref = oracle_full(inp, D=D, init=init)
@@ -83,6 +97,8 @@ def test_short_and_boundary_lengths(algo, L):
 @pytest.mark.parametrize("algo", ALGOS)
 def test_optional_arguments_absent(algo):
     inp = ssd_synth.make_inputs(W[1], seed=9, batch=1, seqlen=513, nheads=4, init_states=True)
+    if not _algo_ok(inp, algo):
+        pytest.skip(f"{algo} path does not take this input")
     y, fin = run_gpu(inp, algo=algo, D=False, init=False, final=False)
     assert fin is None
     y_ref, _ = oracle_full(inp, D=False, init=False)
@@ -109,6 +125,8 @@ def test_varlen_packed_equals_separate_runs(algo):
     segs = [300, 17, 451]
     inp = ssd_synth.make_inputs(W[4], seed=77, seqlen=sum(segs), nheads=4,
                                 init_states=True, segment_lengths=segs)
+    if not _algo_ok(inp, algo):
+        pytest.skip(f"{algo} path does not take this input")
     y, fin = run_gpu(inp, algo=algo)
     cu = inp["cu_seqlens"]
     for s in range(len(segs)):
@@ -127,6 +145,8 @@ def test_varlen_packed_equals_separate_runs(algo):
 @pytest.mark.parametrize("algo", ALGOS)
 def test_split_invariance_through_states(algo):
     inp = ssd_synth.make_inputs(W[3], seed=11, batch=2, seqlen=900, nheads=8)
+    if not _algo_ok(inp, algo):
+        pytest.skip(f"{algo} path does not take this input")
     y, fin = run_gpu(inp, algo=algo)
     t0 = 384
     first, second = dict(inp), dict(inp)
@@ -145,6 +165,8 @@ def test_split_invariance_through_states(algo):
 def test_dt_zero_freezes_state(algo):
     inp = ssd_synth.make_inputs(W[1], seed=3, batch=1, seqlen=300, nheads=2, init_states=True)
     inp["dt"] = torch.zeros_like(inp["dt"])
+    if not _algo_ok(inp, algo):
+        pytest.skip(f"{algo} path does not take this input")
     y, fin = run_gpu(inp, algo=algo)
     assert np.array_equal(fin, inp["initial_states"].numpy())
     _compare_full(inp, algo)
@@ -156,6 +178,8 @@ def test_dt_zero_freezes_state(algo):
 @pytest.mark.parametrize("wi", [1, 2, 3, 4])
 def test_full_size_workload_sampled(algo, wi):
     inp = ssd_synth.make_inputs(W[wi], seed=0)
+    if not _algo_ok(inp, algo):
+        pytest.skip(f"{algo} path does not take this input")
     tol = TOL[inp["dtype"]]
     y, fin = run_gpu(inp, algo=algo)
     assert np.isfinite(y).all()
