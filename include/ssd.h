@@ -150,6 +150,41 @@ SSD_API const char *ssd_status_string(int status);
  * SSD_ALGO_TC), or a negative ssd_status if the shape is rejected. */
 SSD_API int ssd_resolve_algo(const ssd_shape *shape);
 
+/*
+ * ssd_scan() without a workspace: for callers that cannot allocate device
+ * memory when they run the scan -- code running inside another framework's
+ * execution hook (an inference runtime's plugin enqueue, a custom-op
+ * callback) where that framework owns all device allocations, or a
+ * real-time loop that forbids allocation after start-up.  The pages
+ * describing the method have no counterpart to this entry point; it exists
+ * only for such callers.
+ *
+ * The call computes exactly what ssd_scan() computes on its tensor-core
+ * path, using a scratch array that belongs to the library: a static device
+ * array of 32 MiB that every GPU loading the library holds until the
+ * process exits.  The caller passes only inputs and outputs (same meaning,
+ * layout and alignment as ssd_scan(); no cu_seqlens).
+ *   device_status  nullable DEVICE pointer to one int; if given, the call's
+ *                  device status word (SSD_OK or SSD_ERR_DEVICE_TIMEOUT) is
+ *                  copied there on `stream` when the scan's work is done.
+ * Returns SSD_ERR_WORKSPACE, before enqueuing anything, if the shape needs
+ * more scratch than the 32 MiB array holds (the need is
+ * ssd_scan_workspace_size() of the same shape with algo SSD_ALGO_TC), and
+ * SSD_ERR_UNSUPPORTED for shapes the tensor-core path does not take.
+ * Allocates nothing: no cudaMalloc/cudaFree and no allocating library call.
+ * All calls share the one array and it keeps the last call's contents (the
+ * call clears what must start at zero), so calls whose GPU work overlaps --
+ * on different streams or from different host threads -- race; order them,
+ * for example by issuing them on one stream.  The first call on a device,
+ * with that device current, looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture begins.
+ */
+SSD_API int ssd_scan_noalloc(const ssd_shape *shape, const void *x, const float *dt,
+                             const float *A, const void *B, const void *C,
+                             const float *D, const float *initial_states, void *y,
+                             float *final_states, int *device_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

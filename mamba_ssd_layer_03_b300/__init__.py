@@ -76,6 +76,8 @@ def load_library() -> ctypes.CDLL:
     lib.ssd_status_string.restype = ctypes.c_char_p
     lib.ssd_resolve_algo.argtypes = [sp]
     lib.ssd_resolve_algo.restype = ctypes.c_int
+    lib.ssd_scan_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.ssd_scan_noalloc.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -186,6 +188,26 @@ def ssd_scan(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor
         if rc != 0:
             raise SsdError(rc, "ssd_scan (device)")
     return y, fin
+
+
+def ssd_scan_noalloc(x, dt, A, B, C, D=None, chunk_size=256, initial_states=None,
+                     out=None, final_out=None, device_status=None):
+    """Scan on the library's own scratch (no workspace, nothing allocated by
+    the library).  For callers that cannot allocate device memory while the
+    scan runs; outputs may be passed in (``out``, ``final_out``) so that this
+    wrapper allocates nothing either.  Returns (y, final_states or None)."""
+    lib = load_library()
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    shape = make_shape(b, L, H, P, N, G, chunk_size, b, x.dtype, "tc")
+    y = out if out is not None else torch.empty_like(x)
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    rc = lib.ssd_scan_noalloc(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                              _ptr(D), _ptr(initial_states), _ptr(y), _ptr(final_out),
+                              _ptr(device_status), ctypes.c_void_p(stream))
+    if rc != 0:
+        raise SsdError(rc, "ssd_scan_noalloc")
+    return y, final_out
 
 
 def _scan_from_host(x, dt, A, B, C, D, chunk_size, initial_states, cu_seqlens,
