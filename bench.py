@@ -71,7 +71,9 @@ def workload_cost(inp):
 
 
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML in a thread."""
+    """Samples SM clock and clock-event (throttle) reasons while the timed
+    region runs: NVML when the Python bindings are present, else a
+    background `nvidia-smi --query-gpu ... -lms` process."""
 
     REASONS = {
         0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
@@ -81,21 +83,22 @@ class ClockSampler:
     }
 
     def __init__(self, index: int):
-        self.samples = []
-        self.ok = False
+        self.index = index
+        self.samples = []          # (host time, sm MHz, reasons bitmask)
+        self.max_mhz = None
         self._stop = threading.Event()
+        self._proc = None
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
             self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception:  # NVML missing: report nothing rather than guess
-            self.max_mhz = None
-        self.window = None
+            self.source = "nvml"
+        except Exception:
+            self.source = "nvidia-smi"
 
-    def _run(self):
+    def _run_nvml(self):
         nv = self.nv
         while not self._stop.is_set():
             try:
@@ -106,33 +109,57 @@ class ClockSampler:
                 pass
             time.sleep(0.002)
 
+    def _run_smi(self):
+        import subprocess
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        for line in self._proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            try:
+                mhz, mx, rs = float(parts[0]), float(parts[1]), int(parts[2], 16)
+            except (ValueError, IndexError):
+                continue
+            self.max_mhz = mx
+            self.samples.append((time.perf_counter(), mhz, rs))
+            if self._stop.is_set():
+                break
+
     def __enter__(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
-            self.t.start()
+        self.t = threading.Thread(target=self._run_nvml if self.source == "nvml" else self._run_smi,
+                                  daemon=True)
+        self.t.start()
         return self
 
     def __exit__(self, *exc):
         self._stop.set()
-        if self.ok:
-            self.t.join()
+        if self._proc is not None:
+            self._proc.terminate()
+        self.t.join(timeout=5)
 
     def summary(self, t0, t1):
-        if not self.ok or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["nvml_unavailable"]}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no_samples"],
+                    "source": self.source}
         inside = [s for s in self.samples if t0 <= s[0] <= t1]
         note = "in_timed_region"
         if not inside:
-            # the timed region was shorter than the NVML sampling period: use
-            # the samples closest to it
-            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:5]
+            # the timed region was shorter than the sampling period: use the
+            # samples closest to it
+            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
             note = "nearest_to_timed_region"
         mask = 0
         for s in inside:
             mask |= s[2]
         reasons = [n for bit, n in self.REASONS.items() if mask & bit and n != "gpu_idle"]
         return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(inside), "window": note}
+                "reasons": reasons, "samples": len(inside), "window": note,
+                "source": self.source}
 
 
 def time_oracle_sample(inp, budget_s: float):
@@ -223,7 +250,9 @@ def main():
 
     sampler = ClockSampler(local)
     with sampler:
-        time.sleep(0.05)
+        time.sleep(0.3)   # let the sampler start
+        for _ in range(max(args.warmup, 1)):
+            step()
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
@@ -242,7 +271,7 @@ def main():
         t_host1 = time.perf_counter()
         if dist:
             dist.barrier()
-        time.sleep(0.02)
+        time.sleep(0.15)
     total_ms = ev0.elapsed_time(ev1)
     per_step = [a.elapsed_time(b) for a, b in step_ev]
     if dist:
