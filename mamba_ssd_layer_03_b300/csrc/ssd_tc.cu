@@ -331,6 +331,12 @@ k_chunk_state(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ C
         float *Eout = ring_rp + (int64_t)((T.c + 1) & 1) * a.kh * PN + (int64_t)hh * PN;
         const float *Einit = (a.init && hok) ? a.init + ((int64_t)T.r * a.H + h) * PN : nullptr;
         const float decay = hok ? __expf(sm->cs[hh][T.len - 1]) : 0.f;
+        // E_c (bf16, for the output kernel) and the final state are written
+        // from registers here: once the flag below is released, the next
+        // chunk's tile may overwrite this tile's input slot of the ring.
+        bf16 *eb = hok ? a.ebuf + (((int64_t)T.r * a.nc + T.c) * a.H + h) * PN : nullptr;
+        float *fin = (hok && a.final_states && T.c == a.nc - 1)
+                         ? a.final_states + ((int64_t)T.r * a.H + h) * PN : nullptr;
         for (int mt = 0; mt < a.N / 128; ++mt) {
             const int n = mt * 128 + (tid & 127);
 #pragma unroll
@@ -345,7 +351,10 @@ k_chunk_state(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ C
                     float e;
                     if (T.c == 0) e = Einit ? __ldg(Einit + idx) : 0.f;
                     else e = __ldcg(Ein + idx);
-                    __stcg(Eout + idx, decay * e + __uint_as_float(sv[q]));
+                    const float en = decay * e + __uint_as_float(sv[q]);
+                    __stcg(Eout + idx, en);
+                    eb[idx] = __float2bfloat16_rn(e);
+                    if (fin) fin[idx] = en;
                 }
             }
         }
@@ -353,23 +362,6 @@ k_chunk_state(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ C
         tc_fence_before();
         __syncthreads();
         if (tid == 0) st_release(flag, T.c + 1);
-        // off the critical path: E_c in bf16 for the output kernel, final states
-        if (hok) {
-            bf16 *eb = a.ebuf + (((int64_t)T.r * a.nc + T.c) * a.H + h) * PN;
-            float *fin = (a.final_states && T.c == a.nc - 1)
-                             ? a.final_states + ((int64_t)T.r * a.H + h) * PN : nullptr;
-            for (int mt = 0; mt < a.N / 128; ++mt) {
-                const int n = mt * 128 + (tid & 127);
-#pragma unroll 8
-                for (int p = 0; p < 64; ++p) {
-                    const int64_t idx = (int64_t)p * a.N + n;
-                    const float e = (T.c == 0) ? (Einit ? __ldg(Einit + idx) : 0.f) : __ldcg(Ein + idx);
-                    eb[idx] = __float2bfloat16_rn(e);
-                    if (fin) fin[idx] = __ldcg(Eout + idx);
-                }
-            }
-        }
-        __syncthreads();
     }
     tc_fence_before();
     __syncthreads();

@@ -43,6 +43,13 @@ def _compare_full(inp, algo, chunk=None, D=True, init=True):
     ey, ef = rel_err(y, y_ref), rel_err(fin, fin_ref)
     assert ey <= tol, f"y rel err {ey:.3e} > {tol}"
     assert ef <= tol, f"final_states rel err {ef:.3e} > {tol}"
+    if D:
+        # D x is most of |y| at these scales (B, C ~ N(0, 1/N), dt ~ 1e-3..1e-1),
+        # so the bar is checked once more on the scan term alone.
+        y0, _ = run_gpu(inp, chunk=chunk, algo=algo, D=False, init=init, final=False)
+        y0_ref, _ = oracle_full(inp, D=False, init=init)
+        e0 = rel_err(y0, y0_ref)
+        assert e0 <= tol, f"y (D = 0) rel err {e0:.3e} > {tol}"
     return ey, ef
 
 
@@ -92,6 +99,16 @@ def test_chunk_size_independence_bf16(algo, chunk):
 def test_short_and_boundary_lengths(algo, L):
     inp = ssd_synth.make_inputs(W[1], seed=L, batch=2, seqlen=L, nheads=3, init_states=True)
     _compare_full(inp, algo, chunk=64)
+
+
+@pytest.mark.parametrize("chunk", [128, 256])
+@pytest.mark.parametrize("L", [1, 2, 127, 128, 129, 255, 256, 257, 513, 1023])
+def test_short_and_boundary_lengths_tc_chunks(chunk, L):
+    """Lengths around the tensor-core path's 128-token blocks and chunk ends,
+    at the chunk sizes it takes (both paths run)."""
+    inp = ssd_synth.make_inputs(W[1], seed=1000 + L, batch=2, seqlen=L, nheads=4, init_states=True)
+    for algo in ALGOS:
+        _compare_full(inp, algo, chunk=chunk)
 
 
 @pytest.mark.parametrize("algo", ALGOS)
@@ -182,11 +199,14 @@ def test_full_size_workload_sampled(algo, wi):
         pytest.skip(f"{algo} path does not take this input")
     tol = TOL[inp["dtype"]]
     y, fin = run_gpu(inp, algo=algo)
-    assert np.isfinite(y).all()
+    y0, _ = run_gpu(inp, algo=algo, D=False, final=False)
+    assert np.isfinite(y).all() and np.isfinite(y0).all()
     for (s, h) in sample_units(inp, 6, seed=wi):
         yu, fu = oracle_unit(inp, s, h)
+        y0u, _ = oracle_unit(inp, s, h, D=False)
         row, t0, t1, _ = unit_slices(inp, s, h)
         assert rel_err(y[row, t0:t1, h], yu) <= tol, (s, h)
+        assert rel_err(y0[row, t0:t1, h], y0u) <= tol, (s, h, "D = 0")
         assert rel_err(fin[s, h], fu) <= tol, (s, h)
 
 
