@@ -81,10 +81,17 @@ typedef enum ssd_dtype {
 } ssd_dtype;
 
 typedef enum ssd_algo {
-    SSD_ALGO_AUTO = 0,  /* tensor-core path when the shape allows, else SIMT */
-    SSD_ALGO_SIMT = 1,  /* CUDA-core kernels, any supported shape/dtype */
-    SSD_ALGO_TC = 2     /* tcgen05/TMEM/TMA path (bf16 only); UNSUPPORTED if
-                           the shape does not fit it */
+    SSD_ALGO_AUTO = 0,     /* tensor-core path when the shape allows, else SIMT */
+    SSD_ALGO_SIMT = 1,     /* CUDA-core kernels, any supported shape/dtype */
+    SSD_ALGO_TC = 2,       /* tcgen05/TMEM/TMA path (bf16 only): the fused
+                              single-pass kernel for headdim 64 / dstate 128
+                              (any chunk size, packed sequences included),
+                              else the two-pass kernels; UNSUPPORTED if the
+                              shape fits neither */
+    SSD_ALGO_TC_TWOPASS = 3 /* the two-pass tensor-core kernels (chunk-state
+                              scan, then chunk output): bf16, headdim 64,
+                              dstate 128 or 256, chunk 128 or 256, no packed
+                              sequences */
 } ssd_algo;
 
 typedef enum ssd_status {
@@ -146,8 +153,9 @@ SSD_API int ssd_check_device_status(const void *workspace, void *stream);
 /* Static, human-readable name of a status code (never NULL). */
 SSD_API const char *ssd_status_string(int status);
 
-/* Which algorithm ssd_scan() would run for `shape` (SSD_ALGO_SIMT or
- * SSD_ALGO_TC), or a negative ssd_status if the shape is rejected. */
+/* Which algorithm ssd_scan() would run for `shape` (SSD_ALGO_SIMT,
+ * SSD_ALGO_TC for the fused kernel or SSD_ALGO_TC_TWOPASS), or a negative
+ * ssd_status if the shape is rejected. */
 SSD_API int ssd_resolve_algo(const ssd_shape *shape);
 
 /*
@@ -159,8 +167,8 @@ SSD_API int ssd_resolve_algo(const ssd_shape *shape);
  * describing the method have no counterpart to this entry point; it exists
  * only for such callers.
  *
- * The call computes exactly what ssd_scan() computes on its tensor-core
- * path, using a scratch array that belongs to the library: a static device
+ * The call computes exactly what ssd_scan() computes on its two-pass
+ * tensor-core path (SSD_ALGO_TC_TWOPASS), using a scratch array that belongs to the library: a static device
  * array of 32 MiB that every GPU loading the library holds until the
  * process exits.  The caller passes only inputs and outputs (same meaning,
  * layout and alignment as ssd_scan(); no cu_seqlens).
@@ -169,8 +177,9 @@ SSD_API int ssd_resolve_algo(const ssd_shape *shape);
  *                  copied there on `stream` when the scan's work is done.
  * Returns SSD_ERR_WORKSPACE, before enqueuing anything, if the shape needs
  * more scratch than the 32 MiB array holds (the need is
- * ssd_scan_workspace_size() of the same shape with algo SSD_ALGO_TC), and
- * SSD_ERR_UNSUPPORTED for shapes the tensor-core path does not take.
+ * ssd_scan_workspace_size() of the same shape with algo
+ * SSD_ALGO_TC_TWOPASS), and SSD_ERR_UNSUPPORTED for shapes the two-pass
+ * path does not take.
  * Allocates nothing: no cudaMalloc/cudaFree and no allocating library call.
  * All calls share the one array and it keeps the last call's contents (the
  * call clears what must start at zero), so calls whose GPU work overlaps --

@@ -32,7 +32,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libssd.so")
 
 SSD_F32, SSD_BF16 = 0, 1
-ALGOS = {"auto": 0, "simt": 1, "tc": 2}
+ALGOS = {"auto": 0, "simt": 1, "tc": 2, "tc2": 3}
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED",
           3: "SSD_ERR_WORKSPACE", 4: "SSD_ERR_CUDA", 5: "SSD_ERR_DEVICE_TIMEOUT",
           6: "SSD_ERR_DEVICE_INPUT"}
@@ -110,7 +110,7 @@ def resolve_algo(shape: SsdShape) -> str:
     rc = load_library().ssd_resolve_algo(ctypes.byref(shape))
     if rc < 0:
         raise SsdError(-rc, "ssd_resolve_algo")
-    return {1: "simt", 2: "tc"}[rc]
+    return {1: "simt", 2: "tc", 3: "tc2"}[rc]
 
 
 def _ptr(t: Optional[torch.Tensor]):

@@ -32,12 +32,19 @@ int resolve(const ssd_shape *s, Problem &p, int *algo_out) {
     p.H = s->nheads; p.P = s->headdim; p.N = s->dstate; p.G = s->ngroups;
     p.Q = s->chunk_size; p.nseq = s->nseq; p.dtype = s->dtype;
     p.nc = (int)((s->seqlen + s->chunk_size - 1) / s->chunk_size);
+    // SSD_ALGO_TC resolves to the fused kernel when it takes the shape and to
+    // the two-pass kernels otherwise; AUTO prefers tensor cores over SIMT.
     int algo = s->algo;
-    if (algo == SSD_ALGO_AUTO)
-        algo = (tc_supported(p) == SSD_OK) ? SSD_ALGO_TC : SSD_ALGO_SIMT;
+    if (algo == SSD_ALGO_AUTO || algo == SSD_ALGO_TC) {
+        if (fused_supported(p) == SSD_OK) algo = SSD_ALGO_TC;
+        else if (tc_supported(p) == SSD_OK) algo = SSD_ALGO_TC_TWOPASS;
+        else if (algo == SSD_ALGO_AUTO) algo = SSD_ALGO_SIMT;
+        else return SSD_ERR_UNSUPPORTED;
+    }
     int rc;
     if (algo == SSD_ALGO_SIMT) rc = simt_supported(p);
-    else if (algo == SSD_ALGO_TC) rc = tc_supported(p);
+    else if (algo == SSD_ALGO_TC) rc = fused_supported(p);
+    else if (algo == SSD_ALGO_TC_TWOPASS) rc = tc_supported(p);
     else return SSD_ERR_INVALID_ARG;
     if (rc != SSD_OK) return rc;
     *algo_out = algo;
@@ -45,8 +52,22 @@ int resolve(const ssd_shape *s, Problem &p, int *algo_out) {
 }
 
 size_t workspace_for(const Problem &p, int algo) {
-    const size_t body = (algo == SSD_ALGO_TC) ? tc_workspace_bytes(p) : simt_workspace_bytes(p);
+    const size_t body = (algo == SSD_ALGO_TC)          ? fused_workspace_bytes(p)
+                        : (algo == SSD_ALGO_TC_TWOPASS) ? tc_workspace_bytes(p)
+                                                        : simt_workspace_bytes(p);
     return kStatusBytes + body;
+}
+
+// The two-pass kernels take no packed sequences.  A shape with one batch row
+// may come with cu_seqlens, and AUTO then falls back to SIMT, so the
+// workspace asked for covers both.
+size_t workspace_need(const ssd_shape *s, const Problem &p, int algo) {
+    size_t need = workspace_for(p, algo);
+    if (algo == SSD_ALGO_TC_TWOPASS && s->algo == SSD_ALGO_AUTO && p.batch == 1) {
+        const size_t simt = workspace_for(p, SSD_ALGO_SIMT);
+        if (simt > need) need = simt;
+    }
+    return need;
 }
 
 bool aligned(const void *ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
@@ -90,7 +111,7 @@ SSD_API int ssd_scan_workspace_size(const ssd_shape *shape, size_t *bytes) {
     int algo = 0;
     const int rc = resolve(shape, p, &algo);
     if (rc != SSD_OK) return rc;
-    *bytes = workspace_for(p, algo);
+    *bytes = workspace_need(shape, p, algo);
     return SSD_OK;
 }
 
@@ -108,7 +129,11 @@ SSD_API int ssd_scan(const ssd_shape *shape, const void *x, const float *dt, con
     } else if (p.nseq != p.batch) {
         return SSD_ERR_INVALID_ARG;
     }
-    const size_t need = workspace_for(p, algo);
+    const size_t need = workspace_need(shape, p, algo);
+    if (cu_seqlens && algo == SSD_ALGO_TC_TWOPASS) {
+        if (shape->algo != SSD_ALGO_AUTO) return SSD_ERR_UNSUPPORTED;
+        algo = SSD_ALGO_SIMT;
+    }
     if (!workspace || workspace_bytes < need) return SSD_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return SSD_ERR_WORKSPACE;
     const int64_t tokens = p.batch * p.seqlen;
@@ -118,7 +143,7 @@ SSD_API int ssd_scan(const ssd_shape *shape, const void *x, const float *dt, con
         !aligned(dt, 4) || !aligned(A, 4) || !aligned(D, 4) || !aligned(initial_states, 4) ||
         !aligned(final_states, 4) || !aligned(cu_seqlens, 4))
         return SSD_ERR_UNSUPPORTED;
-    if (algo == SSD_ALGO_TC &&
+    if (algo != SSD_ALGO_SIMT &&
         (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
          !aligned(initial_states, 16) || !aligned(final_states, 16)))
         return SSD_ERR_UNSUPPORTED;
@@ -144,7 +169,9 @@ SSD_API int ssd_scan(const ssd_shape *shape, const void *x, const float *dt, con
         }
         return SSD_OK;
     }
-    const cudaError_t e = (algo == SSD_ALGO_TC) ? tc_launch(p) : simt_launch(p);
+    const cudaError_t e = (algo == SSD_ALGO_TC)          ? fused_launch(p)
+                          : (algo == SSD_ALGO_TC_TWOPASS) ? tc_launch(p)
+                                                          : simt_launch(p);
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

@@ -1,0 +1,982 @@
+// Fused single-pass tensor-core path of the SSD forward scan (bf16 x/B/C/y,
+// fp32 dt/A/D/states, headdim 64, dstate 128).
+//
+// The scan is the block decomposition of the semiseparable matrix
+// M = L o (C B^T) (QbitAI article "新架构Mamba更新二代！", sections
+// "统一SSM和注意力机制" and "Mamba-2：更强学习能力，更快训练推理"): masked quadratic
+// products inside a block of tokens plus a linear recurrence of the per-head
+// state across blocks.  Here the recurrence never leaves the chip.
+//
+// Work decomposition.  A "lane" is one sequence and a pair of heads of the
+// same B/C group; its blocks are consecutive 128-token pieces of the
+// sequence.  All blocks of all lanes are numbered lane-major and every CTA
+// takes a contiguous range of that numbering (its "ticket" decides which),
+// so the load is balanced to within one block.  A CTA walks its blocks in
+// order and keeps the running state of its lane in registers.  When a lane
+// is split between two CTAs, the earlier CTA hands the state at the split
+// point to the later one through global memory; every CTA processes the
+// lane it hands off first and the lane it receives last, so the receiver
+// rarely waits.
+//
+// Per block (tokens i, j in [0, 128), heads h of the lane, state H_h[p][n]
+// at the block start, cs_h = within-block cumulative sum of dt*A_h):
+//   CB   = C B^T                                   tensor cores -> TMEM
+//   Ys_h = C H_h^T                                  tensor cores -> TMEM acc
+//   Xw_h = exp(cs_h[127] - cs_h[j]) dt_h[j] x_h[j]   CUDA cores, shared memory
+//   S_h  = B^T Xw_h                                 tensor cores -> TMEM
+//   H_h <- exp(cs_h[127]) H_h + S_h                 CUDA cores, registers
+//   M_h  = CB o exp(cs_h[i] - cs_h[j]) dt_h[j] [j <= i] + D_h [i == j]
+//                                                   CUDA cores, TMEM (bf16)
+//   acc_h = exp(cs_h[i]) Ys_h + M_h x_h            tensor cores (A from TMEM)
+//   y_h  = acc_h                                    -> global (bf16)
+// Every exponent is <= 0.  Adding D_h on the diagonal of M_h folds the skip
+// term D_h x_h into the same product.  The masked block is factored at
+// 32-token sub-blocks: for j in an earlier sub-block with last token e,
+// exp(cs_i - cs_j) = exp(cs_i - cs_e) exp(cs_e - cs_j), so only the sub-block
+// holding i needs one exponential per element.
+//
+// Roles (320 threads, one CTA per SM): warps 0-3 and 4-7 are the two head
+// slots of the lane (TMEM lane = thread index within the warpgroup), warp 8
+// issues the TMA loads, warp 9 issues the MMAs.  They hand work to each
+// other through mbarriers; every wait is bounded in time and, once the
+// call's status word records an error, falls through so that the kernel
+// always finishes.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ssd_device.cuh"
+#include "ssd_internal.h"
+#include "tc_ptx.cuh"
+
+namespace ssd {
+namespace {
+
+using namespace tc;
+typedef __nv_bfloat16 bf16;
+
+constexpr int kB = 128;                    // tokens per block
+constexpr int kThreads = 320;              // 8 compute warps + TMA warp + MMA warp
+constexpr uint32_t kT16 = 16384;           // one 128-row x 128-byte swizzled tile
+constexpr int kP = 64, kN = 128;           // headdim and dstate of this path
+constexpr int kStateFloats = 2 * kP * kN;  // state of one lane (two heads)
+
+struct FArgs {
+    int64_t L;                 // tokens per batch row
+    int H, G, hpg, npg, ptot;  // heads, groups, heads per group, pairs per group, pairs
+    int nseq, varlen, nb_fixed, grid;
+    const float *dt, *A, *D, *init;
+    const int32_t *cu;
+    bf16 *y;
+    float *final_states;
+    int *status;
+    int *ticket;               // ticket counter
+    int *hflag;                // [grid] handoff published by ticket i
+    float *hslot;              // [grid][2][P][N] handoff states
+    const int *seqblk;         // [nseq + 1] prefix of blocks per sequence (varlen)
+};
+
+struct Smem {
+    // [block parity][head][token]: the other warpgroup may still read the
+    // previous block's values while this one writes the next block's
+    float cs[2][2][kB];
+    float dtv[2][2][kB];
+    float vf[2][2][kB];
+    float part[2][4];
+    float dtn[2][2][kB];   // [block parity][head][token]: dt prefetched one block ahead
+    uint64_t c_full, b_full, x_full[2];
+    uint64_t cb_done, s_done, mx_done[2], c_empty, b_empty, x_empty[2], mma_fin;
+    uint64_t hop_ready, xw_ready, m_ready, acc_free[2];
+    uint32_t tmem;
+    int ticket;
+};
+
+constexpr size_t kTileBytes = 12 * (size_t)kT16;  // C, B, X[2], Xw, H_op in 16 KB atoms
+constexpr size_t kSmemBytes = 1024 + kTileBytes + sizeof(Smem);
+
+// ----------------------------------------------------------------------------
+// lanes and blocks
+
+struct Lane {
+    int s, row, h0, nh, g, len, nb;
+    int64_t t0, start;   // first token in the row; first global block index
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ int64_t total_blocks(const FArgs &a) {
+    return a.varlen ? (int64_t)__ldg(a.seqblk + a.nseq) * a.ptot
+                    : (int64_t)a.nseq * a.ptot * a.nb_fixed;
+}
+
+__device__ __forceinline__ Lane lane_info(const FArgs &a, int64_t l) {
+    Lane n;
+    n.s = (int)(l / a.ptot);
+    const int pair = (int)(l % a.ptot);
+    n.g = pair / a.npg;
+    const int k = pair % a.npg;
+    n.h0 = n.g * a.hpg + 2 * k;
+    n.nh = min(2, a.hpg - 2 * k);
+    if (a.varlen) {
+        const int c0 = __ldg(a.cu + n.s), c1 = __ldg(a.cu + n.s + 1);
+        n.row = 0;
+        n.t0 = c0;
+        n.len = max(0, c1 - c0);
+        n.nb = cdiv(n.len, kB);
+        n.start = (int64_t)__ldg(a.seqblk + n.s) * a.ptot + (int64_t)pair * n.nb;
+    } else {
+        n.row = n.s;
+        n.t0 = 0;
+        n.len = (int)a.L;
+        n.nb = a.nb_fixed;
+        n.start = l * a.nb_fixed;
+    }
+    return n;
+}
+
+// Lane that holds global block g (0 <= g < total_blocks).
+__device__ __forceinline__ int64_t find_lane(const FArgs &a, int64_t g) {
+    if (!a.varlen) return g / a.nb_fixed;
+    int lo = 0, hi = a.nseq - 1;
+    while (lo < hi) {   // largest s with seqblk[s] * ptot <= g
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)__ldg(a.seqblk + mid) * a.ptot <= g) lo = mid; else hi = mid - 1;
+    }
+    const int64_t base = (int64_t)__ldg(a.seqblk + lo) * a.ptot;
+    const int nb = max(1, __ldg(a.seqblk + lo + 1) - __ldg(a.seqblk + lo));
+    const int64_t pair = min((int64_t)a.ptot - 1, (g - base) / nb);
+    return (int64_t)lo * a.ptot + pair;
+}
+
+// The blocks of one CTA: range [g0, g1) of the global numbering, visited
+// lane by lane in the order last lane, middle lanes, first lane.
+struct Walk {
+    int64_t g0, g1, l0, l1, nl;
+    int64_t k;      // segment index in visiting order
+    Lane ln;
+    int b, b_begin, b_end;
+    bool valid;
+};
+
+__device__ __forceinline__ int64_t seg_lane(const Walk &w, int64_t k) {
+    if (w.l0 == w.l1 || k == 0) return w.l1;
+    if (k == w.nl - 1) return w.l0;
+    return w.l0 + k;
+}
+
+__device__ __forceinline__ void walk_load_seg(const FArgs &a, Walk &w) {
+    while (w.k < w.nl) {
+        w.ln = lane_info(a, seg_lane(w, w.k));
+        const int64_t lo = max64(w.g0, w.ln.start), hi = min64(w.g1, w.ln.start + w.ln.nb);
+        if (lo < hi) {
+            w.b_begin = (int)(lo - w.ln.start);
+            w.b_end = (int)(hi - w.ln.start);
+            w.b = w.b_begin;
+            w.valid = true;
+            return;
+        }
+        ++w.k;
+    }
+    w.valid = false;
+}
+
+__device__ __forceinline__ void walk_init(const FArgs &a, Walk &w, int ticket) {
+    const int64_t T = total_blocks(a);
+    w.g0 = (int64_t)ticket * T / a.grid;
+    w.g1 = (int64_t)(ticket + 1) * T / a.grid;
+    w.valid = false;
+    if (w.g0 >= w.g1) return;
+    w.l0 = find_lane(a, w.g0);
+    w.l1 = find_lane(a, w.g1 - 1);
+    w.nl = w.l1 - w.l0 + 1;
+    w.k = 0;
+    walk_load_seg(a, w);
+}
+
+__device__ __forceinline__ void walk_next(const FArgs &a, Walk &w) {
+    if (++w.b < w.b_end) return;
+    ++w.k;
+    walk_load_seg(a, w);
+}
+
+// ----------------------------------------------------------------------------
+// small helpers
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_i(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_i(int *p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// mbarrier.try_wait with a suspend-time hint: a waiting thread sleeps (and
+// issues nothing) until the phase completes or about `ns` have passed.
+__device__ __forceinline__ bool try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait.  Once it has waited far longer than any healthy step takes
+// (20 us), it also gives up as soon as the call's status word records an
+// error, so that a failed call finishes quickly; the status word is not read
+// before then because that global read would delay the wake-up.
+__device__ __forceinline__ bool fwait(uint64_t *bar, uint32_t parity, int *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        for (int i = 0; i < 16; ++i)
+            if (try_wait_sleep(bar, parity, 2000)) return true;
+        const uint64_t dt = globaltimer_ns() - t0;
+        if (dt > 20000ull && status_bad(status)) return false;
+        if (dt > kWaitLimitNs) {
+            set_status(status, SSD_ERR_DEVICE_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Plain bounded wait used only while draining at exit.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > 50000000ull) return;
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// TMEM column of k-step kk (tokens j in [16 kk, 16 kk + 16)) of the masked
+// block of head hh: M is written over C B^T in place, each 32-column fp32
+// chunk of C B^T (j in [32 m, 32 m + 32)) turning into the two heads'
+// 16-column bf16 pieces of the same j range.
+__device__ __forceinline__ uint32_t m_col(int kk, int hh) {
+    return (uint32_t)(32 * (kk >> 1) + 16 * hh + 8 * (kk & 1));
+}
+
+__device__ __forceinline__ uint4 scale_bf16x8(uint4 u, float s) {
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = bf2_to_f2(w[q]);
+        w[q] = pack_bf16x2(f.x * s, f.y * s);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ----------------------------------------------------------------------------
+// the kernel
+
+__global__ void __launch_bounds__(kThreads, 1)
+k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
+            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmY,
+            FArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *sC = base;                  // [n atom][128 rows][64]        32 KB
+    uint8_t *sB = sC + 2 * kT16;         // [n atom][128 rows][64]        32 KB
+    uint8_t *sX = sB + 2 * kT16;         // [slot][head][128 rows][64]    64 KB
+    uint8_t *sXw = sX + 4 * kT16;        // [head][128 rows][64]          32 KB
+    uint8_t *sH = sXw + 2 * kT16;        // [head][128 n rows][64 p]      32 KB
+    Smem *sm = (Smem *)(sH + 2 * kT16);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        mbar_init(&sm->c_full, 1); mbar_init(&sm->b_full, 1);
+        mbar_init(&sm->x_full[0], 1); mbar_init(&sm->x_full[1], 1);
+        mbar_init(&sm->cb_done, 1); mbar_init(&sm->s_done, 1);
+        mbar_init(&sm->mx_done[0], 1); mbar_init(&sm->mx_done[1], 1);
+        mbar_init(&sm->c_empty, 1); mbar_init(&sm->b_empty, 1);
+        mbar_init(&sm->x_empty[0], 1); mbar_init(&sm->x_empty[1], 1);
+        mbar_init(&sm->mma_fin, 1);
+        mbar_init(&sm->hop_ready, 256); mbar_init(&sm->xw_ready, 256);
+        mbar_init(&sm->m_ready, 256);
+        mbar_init(&sm->acc_free[0], 256); mbar_init(&sm->acc_free[1], 256);
+        fence_mbar_init();
+        prefetch_tmap(&tmX); prefetch_tmap(&tmB); prefetch_tmap(&tmC); prefetch_tmap(&tmY);
+        sm->ticket = atomicAdd(a.ticket, 1);
+    }
+    if (warp == 0) { tmem_alloc(&sm->tmem, 512); tmem_relinquish(); }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = sm->tmem;
+    const uint32_t R_cb = tbase, R_H = tbase + 128;
+    const int ticket = sm->ticket;
+    const bool run = !status_bad(a.status);
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0 && run) {
+            Walk w;
+            walk_init(a, w, ticket);
+            uint32_t k = 0;
+            for (; w.valid; walk_next(a, w), ++k) {
+                const int tok = (int)(w.ln.t0 + (int64_t)w.b * kB);
+                const int slot = k & 1;
+                if (k >= 2) fwait(&sm->x_empty[slot], ((k >> 1) + 1) & 1, a.status);
+                for (int s = 0; s < 2; ++s)
+                    tma_load_4d(sX + (size_t)(slot * 2 + s) * kT16, &tmX, &sm->x_full[slot], 0,
+                                w.ln.h0 + s, tok, w.ln.row);
+                mbar_arrive_expect_tx(&sm->x_full[slot], 2 * kT16);
+                if (k >= 1) fwait(&sm->c_empty, (k - 1) & 1, a.status);
+                for (int nb = 0; nb < 2; ++nb)
+                    tma_load_4d(sC + nb * kT16, &tmC, &sm->c_full, nb * 64, w.ln.g, tok, w.ln.row);
+                mbar_arrive_expect_tx(&sm->c_full, 2 * kT16);
+                if (k >= 1) fwait(&sm->b_empty, (k - 1) & 1, a.status);
+                for (int nb = 0; nb < 2; ++nb)
+                    tma_load_4d(sB + nb * kT16, &tmB, &sm->b_full, nb * 64, w.ln.g, tok, w.ln.row);
+                mbar_arrive_expect_tx(&sm->b_full, 2 * kT16);
+            }
+            // let every copy this thread started land before the CTA exits
+            if (k >= 1) {
+                drain_wait(&sm->c_full, (k - 1) & 1);
+                drain_wait(&sm->b_full, (k - 1) & 1);
+                drain_wait(&sm->x_full[(k - 1) & 1], ((k - 1) >> 1) & 1);
+            }
+            if (k >= 2) drain_wait(&sm->x_full[k & 1], ((k - 2) >> 1) & 1);
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0 && run) {
+            const uint32_t id_cb = idesc_bf16_f32(128, 128, 0, 0);
+            const uint32_t id_ys = idesc_bf16_f32(128, 128, 0, 1);
+            const uint32_t id_s = idesc_bf16_f32(128, 128, 1, 1);
+            const uint32_t id_mx = idesc_bf16_f32(128, 64, 0, 1);
+            const uint32_t sc = smem_u32(sC), sbb = smem_u32(sB), sxw = smem_u32(sXw),
+                           sh = smem_u32(sH), sx = smem_u32(sX);
+            Walk w;
+            walk_init(a, w, ticket);
+            uint32_t k = 0;
+            for (; w.valid; walk_next(a, w), ++k) {
+                const int slot = k & 1;
+                const uint32_t R_acc = tbase + 256 + 128 * slot;
+                fwait(&sm->c_full, k & 1, a.status);
+                fwait(&sm->b_full, k & 1, a.status);
+                tc_fence_after();
+                // CB = C B^T (over the previous block's M, read by its last product)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * kT16 + (uint32_t)(kk & 3) * 32;
+                    mma_ss(R_cb, smem_desc(sc + off, 16, 1024, kSwizzle128B),
+                           smem_desc(sbb + off, 16, 1024, kSwizzle128B), id_cb, kk > 0);
+                }
+                // Ys = C H^T (both heads stacked along N)
+                fwait(&sm->hop_ready, k & 1, a.status);
+                if (k >= 2) fwait(&sm->acc_free[slot], ((k >> 1) + 1) & 1, a.status);
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * kT16 + (uint32_t)(kk & 3) * 32;
+                    mma_ss(R_acc, smem_desc(sc + off, 16, 1024, kSwizzle128B),
+                           smem_desc(sh + kk * 2048, kT16, 1024, kSwizzle128B), id_ys, kk > 0);
+                }
+                mma_commit(&sm->cb_done);
+                mma_commit(&sm->c_empty);
+                // S = B^T Xw (rows n, columns (head, p))
+                fwait(&sm->xw_ready, k & 1, a.status);
+                fwait(&sm->x_full[slot], (k >> 1) & 1, a.status);
+                tc_fence_after();
+                // H <- (decay H, already in TMEM) + B^T Xw
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(R_H, smem_desc(sbb + kk * 2048, kT16, 1024, kSwizzle128B),
+                           smem_desc(sxw + kk * 2048, kT16, 1024, kSwizzle128B), id_s, 1);
+                mma_commit(&sm->s_done);
+                mma_commit(&sm->b_empty);
+                // acc_h += M_h x_h (M from TMEM)
+                fwait(&sm->m_ready, k & 1, a.status);
+                tc_fence_after();
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(R_acc + hh * 64, R_cb + m_col(kk, hh),
+                               smem_desc(sx + (uint32_t)(slot * 2 + hh) * kT16 + kk * 2048, kT16,
+                                         1024, kSwizzle128B),
+                               id_mx, 1);
+                mma_commit(&sm->mx_done[slot]);
+                mma_commit(&sm->x_empty[slot]);
+            }
+            // every MMA this thread issued has completed before TMEM is freed
+            mma_commit(&sm->mma_fin);
+            drain_wait(&sm->mma_fin, 0);
+        }
+    } else if (run) {
+        // ------------------------------------------------------------ compute
+        // Warpgroup h: thread t is TMEM lane t, i.e. token row i = t of the
+        // block for C B^T, M and the outputs, and state row n = t for H.  For
+        // the state, the scan and the outputs the warpgroup works on head h of
+        // the lane; for the masked block on C B^T columns [64 h, 64 h + 64)
+        // for both heads.
+        const int h = warp >> 2;
+        const int t = tid & 127;
+        const int wq = warp & 3;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const int bar_wg = 1 + h;
+
+        Walk w;
+        walk_init(a, w, ticket);
+        // dt of this thread's token and head in block b of lane ln, copied
+        // into dtn[par][h][t] asynchronously (cp.async: barriers do not wait
+        // for it); zero outside the sequence or the lane's heads
+        auto prefetch_dt = [&](const Lane &ln, int b, int par) {
+            float *dst = &sm->dtn[par][h][t];
+            const int i = b * kB + t;
+            if (h < ln.nh && i < ln.len) {
+                const float *src = a.dt + ((int64_t)ln.row * a.L + ln.t0 + i) * a.H + ln.h0 + h;
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)),
+                             "l"(src) : "memory");
+            } else {
+                *dst = 0.f;
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        bool have_next = false;
+        float Ah = 0.f, D0 = 0.f, D1 = 0.f;
+
+        // previous block, for the deferred epilogue: how its y leaves the chip
+        // (0: no valid head here, 1: TMA store of the whole tile, 2: direct
+        // stores of the rows inside the sequence), where, and this thread's row
+        int prev_mode = 0, prev_head = 0, prev_tok = 0, prev_row = 0;
+        int64_t prev_y = -1;
+        bool pend_store = false;   // a TMA store of y still reads this half of Xw
+        // y of block kk: acc (TMEM) -> bf16 -> this head's half of the Xw
+        // buffer (free once the S product of the following block has read
+        // it; the caller has waited for that) -> TMA store.
+        auto epilogue = [&](uint32_t kk) {
+            const int ps = kk & 1;
+            fwait(&sm->mx_done[ps], (kk >> 1) & 1, a.status);
+            tc_fence_after();
+            const uint32_t R_prev = tbase + 256 + 128 * ps;
+            uint8_t *stile = sXw + (size_t)h * kT16;
+            uint8_t *srow = stile + t * 128;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t v[32];
+                tmem_ld32(R_prev + lane_off + h * 64 + half * 32, v);
+                tmem_ld_wait();
+                uint4 pk[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    pk[c] = make_uint4(
+                        pack_bf16x2(__uint_as_float(v[8 * c]), __uint_as_float(v[8 * c + 1])),
+                        pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3])),
+                        pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5])),
+                        pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])));
+                if (prev_mode == 1) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *(uint4 *)(srow + (((half * 4 + c) ^ (t & 7)) << 4)) = pk[c];
+                } else if (prev_mode == 2 && prev_y >= 0) {
+                    uint4 *dst = (uint4 *)(a.y + prev_y + half * 32);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) dst[c] = pk[c];
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&sm->acc_free[ps]);
+            if (prev_mode == 1) fence_proxy_async_smem();
+            named_bar(bar_wg, 128);
+            if (t == 0 && prev_mode == 1) {
+                tma_store_4d(&tmY, stile, 0, prev_head, prev_tok, prev_row);
+                tma_store_commit();
+                pend_store = true;
+            }
+        };
+
+        uint32_t k = 0;
+        for (; w.valid; walk_next(a, w), ++k) {
+            const Lane &ln = w.ln;
+            const bool hv = h < ln.nh;
+            const int head = ln.h0 + (hv ? h : 0);
+            const int slot = k & 1;
+            const uint32_t R_acc = tbase + 256 + 128 * slot;
+            const int i0 = w.b * kB;
+            const bool tv = hv && (i0 + t < ln.len);
+            const bool seg_start = w.b == w.b_begin;
+            if (seg_start) {
+                Ah = hv ? __ldg(a.A + head) : 0.f;
+                D0 = a.D ? __ldg(a.D + ln.h0) : 0.f;
+                D1 = (a.D && ln.nh > 1) ? __ldg(a.D + ln.h0 + 1) : 0.f;
+            }
+
+            // (a) dt and the within-block cumulative decay cs of head h
+            if (!have_next) prefetch_dt(ln, w.b, slot);
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            const float d = sm->dtn[slot][h][t];
+            have_next = w.b + 1 < w.b_end;
+            if (have_next) prefetch_dt(ln, w.b + 1, slot ^ 1);
+            float incl = d * Ah;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            if (lane == 31) sm->part[h][wq] = incl;
+            named_bar(bar_wg, 128);
+            {
+                const float p0 = sm->part[h][0], p1 = sm->part[h][1], p2 = sm->part[h][2],
+                            p3 = sm->part[h][3];
+                incl += (wq > 0 ? p0 : 0.f) + (wq > 1 ? p1 : 0.f) + (wq > 2 ? p2 : 0.f);
+                const float cs_last = ((p0 + p1) + p2) + p3;
+                const float sub_end = __shfl_sync(0xffffffffu, incl, 31);
+                sm->cs[slot][h][t] = incl;
+                sm->dtv[slot][h][t] = d;
+                sm->vf[slot][h][t] = __expf(sub_end - incl) * d;
+                // reuse part[] only after every thread has read it
+                const float w_t = __expf(fminf(cs_last - incl, 0.f)) * d;
+                const float decay = __expf(cs_last);
+
+                // (d) H_k -> H_op (bf16, operand of C H^T) and H <- decay H_k
+                //     in TMEM, ready for the S product to accumulate on
+                const float *init_src = nullptr;
+                bool from_slot = false;
+                if (seg_start) {
+                    if (w.b_begin > 0) {
+                        // state at the split point, handed over by the previous ticket
+                        const int *flag = a.hflag + (ticket - 1);
+                        const uint64_t tw = globaltimer_ns();
+                        while (ld_acquire_i(flag) == 0) {
+                            if (status_bad(a.status)) break;
+                            if (globaltimer_ns() - tw > kWaitLimitNs) {
+                                set_status(a.status, SSD_ERR_DEVICE_TIMEOUT);
+                                break;
+                            }
+                            __nanosleep(64);
+                        }
+                        init_src = a.hslot + (size_t)(ticket - 1) * kStateFloats + h * kP * kN;
+                        from_slot = true;
+                    } else if (a.init && hv) {
+                        init_src = a.init + ((int64_t)ln.s * a.H + head) * kP * kN;
+                    }
+                } else {
+                    fwait(&sm->s_done, (k - 1) & 1, a.status);
+                    tc_fence_after();
+                }
+                uint8_t *hrow = sH + h * kT16 + t * 128;
+                {
+                    uint32_t v[2][32];
+                    if (seg_start) {
+#pragma unroll
+                        for (int half = 0; half < 2; ++half)
+#pragma unroll
+                            for (int q = 0; q < 32; ++q) {
+                                float e = 0.f;
+                                if (hv && init_src) {
+                                    const float *src = init_src + (half * 32 + q) * kN + t;
+                                    e = from_slot ? __ldcg(src) : __ldg(src);
+                                }
+                                v[half][q] = __float_as_uint(e);
+                            }
+                    } else {
+                        tmem_ld32(R_H + lane_off + h * 64, v[0]);
+                        tmem_ld32(R_H + lane_off + h * 64 + 32, v[1]);
+                        tmem_ld_wait();
+                    }
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            *(uint4 *)(hrow + (((half * 4 + c) ^ (t & 7)) << 4)) = make_uint4(
+                                pack_bf16x2(__uint_as_float(v[half][8 * c]), __uint_as_float(v[half][8 * c + 1])),
+                                pack_bf16x2(__uint_as_float(v[half][8 * c + 2]), __uint_as_float(v[half][8 * c + 3])),
+                                pack_bf16x2(__uint_as_float(v[half][8 * c + 4]), __uint_as_float(v[half][8 * c + 5])),
+                                pack_bf16x2(__uint_as_float(v[half][8 * c + 6]), __uint_as_float(v[half][8 * c + 7])));
+#pragma unroll
+                        for (int q = 0; q < 32; ++q)
+                            v[half][q] = __float_as_uint(decay * __uint_as_float(v[half][q]));
+                        tmem_st32(R_H + lane_off + h * 64 + half * 32, v[half]);
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&sm->hop_ready);
+
+                // (b) Xw_h row t = w_t x_h row t; visit the row's eight 16-byte
+                //     chunks starting at a different one in each of 8 lanes
+                fwait(&sm->x_full[slot], (k >> 1) & 1, a.status);
+                if (t == 0 && pend_store) {
+                    tma_store_wait_read0();
+                    pend_store = false;
+                }
+                named_bar(bar_wg, 128);   // the y store has read this half of Xw
+                {
+                    const uint4 *src = (const uint4 *)(sX + (size_t)(slot * 2 + h) * kT16 + t * 128);
+                    uint4 *dst = (uint4 *)(sXw + h * kT16 + t * 128);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int pc = c ^ (t & 7);
+                        dst[pc] = scale_bf16x8(src[pc], w_t);
+                    }
+                }
+                tmem_st_wait();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&sm->xw_ready);
+            }
+
+            // (e) masked block, in place over C B^T: this warpgroup turns
+            //     columns j in [64 h, 64 h + 64) into both heads' M pieces;
+            //     then acc_h *= exp(cs_h[i]) for head h
+            fwait(&sm->cb_done, k & 1, a.status);
+            named_bar(3, 256);        // cs, dtv, vf of both heads are visible
+            tc_fence_after();
+            {
+                const int i = t;
+                const int ib = wq;
+                const float(*cs)[kB] = sm->cs[slot];
+                const float(*vfs)[kB] = sm->vf[slot];
+                const float(*dts)[kB] = sm->dtv[slot];
+                const float cs0 = cs[0][i], cs1 = cs[1][i];
+#pragma unroll 1
+                for (int mm = 0; mm < 2; ++mm) {
+                    const int m = 2 * h + mm;
+                    uint32_t pk0[16], pk1[16];
+                    if (m > ib) {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) { pk0[q] = 0u; pk1[q] = 0u; }
+                    } else {
+                        uint32_t v[32];
+                        tmem_ld32(R_cb + lane_off + m * 32, v);
+                        tmem_ld_wait();
+                        if (m < ib) {
+                            const float u0 = __expf(cs0 - cs[0][m * 32 + 31]);
+                            const float u1 = __expf(cs1 - cs[1][m * 32 + 31]);
+                            const float *vf0 = vfs[0] + m * 32, *vf1 = vfs[1] + m * 32;
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) {
+                                const float c0 = __uint_as_float(v[2 * q]), c1 = __uint_as_float(v[2 * q + 1]);
+                                pk0[q] = pack_bf16x2(c0 * u0 * vf0[2 * q], c1 * u0 * vf0[2 * q + 1]);
+                                pk1[q] = pack_bf16x2(c0 * u1 * vf1[2 * q], c1 * u1 * vf1[2 * q + 1]);
+                            }
+                        } else {
+                            // sub-block holding i: j <= i.  While the sub-block's
+                            // total decay R = cs[start] - cs[end] stays below 80,
+                            // exp(cs_i - cs_j) = exp(cs_i - cs_end) exp(cs_end - cs_j)
+                            // with the first factor in [1, e^R] and the second
+                            // (inside vf) in [e^-R, 1]: no overflow and no
+                            // subnormal.  Otherwise one exponential per element.
+                            const int li = i & 31;
+                            const float *cj0 = cs[0] + m * 32, *cj1 = cs[1] + m * 32;
+                            const float ref0 = (m == 0) ? 0.f : cs[0][m * 32 - 1];
+                            const float ref1 = (m == 0) ? 0.f : cs[1][m * 32 - 1];
+                            const bool fast = (ref0 - cj0[31] < 80.f) && (ref1 - cj1[31] < 80.f);
+                            if (fast) {
+                                const float u0 = __expf(cs0 - cj0[31]);
+                                const float u1 = __expf(cs1 - cj1[31]);
+                                const float *vf0 = vfs[0] + m * 32, *vf1 = vfs[1] + m * 32;
+#pragma unroll
+                                for (int q = 0; q < 16; ++q) {
+                                    const int j0 = 2 * q, j1 = 2 * q + 1;
+                                    const float c0 = (j0 <= li) ? __uint_as_float(v[j0]) : 0.f;
+                                    const float c1 = (j1 <= li) ? __uint_as_float(v[j1]) : 0.f;
+                                    float a0 = c0 * u0 * vf0[j0], a1 = c1 * u0 * vf0[j1];
+                                    float b0 = c0 * u1 * vf1[j0], b1 = c1 * u1 * vf1[j1];
+                                    if (j0 == li) { a0 += D0; b0 += D1; }
+                                    if (j1 == li) { a1 += D0; b1 += D1; }
+                                    pk0[q] = pack_bf16x2(a0, a1);
+                                    pk1[q] = pack_bf16x2(b0, b1);
+                                }
+                            } else {
+                                const float *dj0 = dts[0] + m * 32, *dj1 = dts[1] + m * 32;
+#pragma unroll
+                                for (int q = 0; q < 16; ++q) {
+                                    const int j0 = 2 * q, j1 = 2 * q + 1;
+                                    const float c0 = __uint_as_float(v[j0]), c1 = __uint_as_float(v[j1]);
+                                    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+                                    if (j0 <= li) {
+                                        a0 = c0 * __expf(cs0 - cj0[j0]) * dj0[j0];
+                                        b0 = c0 * __expf(cs1 - cj1[j0]) * dj1[j0];
+                                    }
+                                    if (j1 <= li) {
+                                        a1 = c1 * __expf(cs0 - cj0[j1]) * dj0[j1];
+                                        b1 = c1 * __expf(cs1 - cj1[j1]) * dj1[j1];
+                                    }
+                                    if (j0 == li) { a0 += D0; b0 += D1; }
+                                    if (j1 == li) { a1 += D0; b1 += D1; }
+                                    pk0[q] = pack_bf16x2(a0, a1);
+                                    pk1[q] = pack_bf16x2(b0, b1);
+                                }
+                            }
+                        }
+                    }
+                    tmem_st16(R_cb + lane_off + m * 32, pk0);
+                    tmem_st16(R_cb + lane_off + m * 32 + 16, pk1);
+                }
+                const float e = __expf(h == 0 ? cs0 : cs1);
+                {
+                    uint32_t v[32], u[32];
+                    tmem_ld32(R_acc + lane_off + h * 64, v);
+                    tmem_ld32(R_acc + lane_off + h * 64 + 32, u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        v[q] = __float_as_uint(__uint_as_float(v[q]) * e);
+                        u[q] = __float_as_uint(__uint_as_float(u[q]) * e);
+                    }
+                    tmem_st32(R_acc + lane_off + h * 64, v);
+                    tmem_st32(R_acc + lane_off + h * 64 + 32, u);
+                }
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            mbar_arrive(&sm->m_ready);
+
+            // (c) epilogue of the previous block, staged in Xw once the S
+            //     product of this block has read it
+            fwait(&sm->s_done, k & 1, a.status);
+            tc_fence_after();
+            if (k >= 1) epilogue(k - 1);
+
+            // end of this CTA's part of the lane: the state after the block
+            if (w.b + 1 == w.b_end) {
+                const bool fin = w.b_end == ln.nb;
+                float *dst = nullptr;
+                if (fin) {
+                    if (a.final_states && hv)
+                        dst = a.final_states + ((int64_t)ln.s * a.H + head) * kP * kN;
+                } else {
+                    dst = a.hslot + (size_t)ticket * kStateFloats + h * kP * kN;
+                }
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v[32];
+                    tmem_ld32(R_H + lane_off + h * 64 + half * 32, v);
+                    tmem_ld_wait();
+                    if (dst) {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) __stcg(dst + (half * 32 + q) * kN + t, __uint_as_float(v[q]));
+                    }
+                }
+                tc_fence_before();
+                if (!fin) {
+                    __threadfence();
+                    // all 256 compute threads have stored: publish
+                    named_bar(3, 256);
+                    if (tid == 0) st_release_i(a.hflag + ticket, 1);
+                }
+            }
+
+            prev_y = tv ? (((int64_t)ln.row * a.L + ln.t0 + i0 + t) * a.H + head) * kP : -1;
+            prev_head = head;
+            prev_tok = (int)(ln.t0 + i0);
+            prev_row = ln.row;
+            // rows past the sequence end may be stored by TMA only where they
+            // are also past the end of the batch row (TMA drops those)
+            prev_mode = !hv ? 0 : (i0 + kB <= ln.len || ln.t0 + ln.len >= a.L) ? 1 : 2;
+        }
+        // epilogue of the last block (its S product has completed: the
+        // lane's end waited for it); the y stores land before exit
+        if (k >= 1) {
+            if (t == 0 && pend_store) tma_store_wait_read0();
+            named_bar(bar_wg, 128);
+            epilogue(k - 1);
+        }
+        if (t == 0) tma_store_wait0();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+// Varlen set-up: blocks per sequence (exclusive prefix) and the final states
+// of empty sequences (their initial states).  One CTA.
+__global__ void k_fused_varlen_setup(FArgs a, int P, int N) {
+    if (status_bad(a.status)) return;
+    __shared__ int carry;
+    __shared__ int warp_sum[32];
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    int *seqblk = const_cast<int *>(a.seqblk);
+    for (int s0 = 0; s0 < a.nseq; s0 += blockDim.x) {
+        const int s = s0 + threadIdx.x;
+        int nb = 0;
+        if (s < a.nseq) nb = cdiv(max(0, __ldg(a.cu + s + 1) - __ldg(a.cu + s)), kB);
+        // block-wide exclusive scan of nb
+        const int ln = threadIdx.x & 31, wp = threadIdx.x >> 5;
+        int v = nb;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, v, off);
+            if (ln >= off) v += o;
+        }
+        if (ln == 31) warp_sum[wp] = v;
+        __syncthreads();
+        int pre = carry;
+        for (int q = 0; q < wp; ++q) pre += warp_sum[q];
+        if (s < a.nseq) seqblk[s] = pre + v - nb;
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry = pre + v;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) seqblk[a.nseq] = carry;
+    // empty sequences: final = initial (or zero)
+    if (a.final_states) {
+        const int PN = P * N;
+        for (int s = 0; s < a.nseq; ++s) {
+            if (__ldg(a.cu + s + 1) > __ldg(a.cu + s)) continue;
+            for (int e = threadIdx.x; e < a.H * PN; e += blockDim.x) {
+                const int64_t idx = (int64_t)s * a.H * PN + e;
+                a.final_states[idx] = a.init ? a.init[idx] : 0.f;
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    }
+    return fn;
+}
+
+// bf16 map of a 4-d tensor, dims[0] innermost; 128-byte swizzle.
+bool make_map4(CUtensorMap *m, const void *ptr, const uint64_t *dims, const uint32_t *box) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gd[4], gs[3];
+    cuuint32_t bx[4], es[4];
+    uint64_t stride = 2;
+    for (int i = 0; i < 4; ++i) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i > 0) gs[i - 1] = stride;
+        stride *= dims[i];
+    }
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), gd, gs, bx, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 148;
+}
+
+struct FLayout {
+    size_t hdr, slots, seqblk, total;
+    int grid;
+};
+
+int64_t lanes_of(const Problem &p) {
+    const int hpg = p.H / p.G;
+    return (int64_t)p.nseq * p.G * ((hpg + 1) / 2);
+}
+
+// Grid: at most one CTA per SM, and never more CTAs than blocks (so that no
+// range is empty).  Without packing, lanes >= grid also keeps every range at
+// least one lane long.  The workspace always has room for one handoff slot
+// per SM, so its size does not depend on cu_seqlens.
+FLayout fused_layout(const Problem &p) {
+    FLayout w{};
+    const int hpg = p.H / p.G;
+    const int64_t ptot = (int64_t)p.G * ((hpg + 1) / 2);
+    const int64_t sms = sm_count();
+    int64_t grid;
+    if (p.cu) grid = min64(sms, ptot * ((p.seqlen + kB - 1) / kB));
+    else grid = min64(sms, lanes_of(p));
+    w.grid = (int)max64(1, grid);
+    size_t off = 0;
+    w.hdr = off;     // ticket (4 B) + flags
+    off = align_up(off + 256 + (size_t)sms * sizeof(int), 256);
+    w.slots = off;
+    off = align_up(off + (size_t)sms * kStateFloats * sizeof(float), 256);
+    w.seqblk = off;
+    off = align_up(off + (size_t)(p.nseq + 1) * sizeof(int), 256);
+    w.total = off;
+    return w;
+}
+
+}  // namespace
+
+size_t fused_workspace_bytes(const Problem &p) { return fused_layout(p).total; }
+
+int fused_supported(const Problem &p) {
+    if (p.dtype != SSD_BF16 || p.P != kP || p.N != kN) return SSD_ERR_UNSUPPORTED;
+    if (!encode_fn()) return SSD_ERR_UNSUPPORTED;
+    return SSD_OK;
+}
+
+cudaError_t fused_launch(const Problem &p) {
+    const FLayout w = fused_layout(p);
+    FArgs a{};
+    a.L = p.seqlen;
+    a.H = p.H; a.G = p.G; a.hpg = p.H / p.G; a.npg = (a.hpg + 1) / 2; a.ptot = p.G * a.npg;
+    a.nseq = p.nseq;
+    a.varlen = p.cu != nullptr;
+    a.nb_fixed = (int)((p.seqlen + kB - 1) / kB);
+    a.grid = w.grid;
+    a.dt = p.dt; a.A = p.A; a.D = p.D; a.init = p.init; a.cu = p.cu;
+    a.y = (bf16 *)p.y;
+    a.final_states = p.final_states;
+    a.status = p.status;
+    a.ticket = (int *)(p.ws + w.hdr);
+    a.hflag = (int *)(p.ws + w.hdr + 256);
+    a.hslot = (float *)(p.ws + w.slots);
+    a.seqblk = (const int *)(p.ws + w.seqblk);
+
+    cudaError_t e = cudaMemsetAsync(p.ws + w.hdr, 0, w.slots - w.hdr, p.stream);
+    if (e != cudaSuccess) return e;
+
+    CUtensorMap tmX, tmB, tmC, tmY;
+    const uint64_t L = (uint64_t)p.seqlen, b = (uint64_t)p.batch;
+    const uint64_t dx[4] = {(uint64_t)p.P, (uint64_t)p.H, L, b};
+    const uint64_t dbc[4] = {(uint64_t)p.N, (uint64_t)p.G, L, b};
+    const uint32_t box[4] = {64, 1, (uint32_t)kB, 1};
+    if (!make_map4(&tmX, p.x, dx, box) || !make_map4(&tmB, p.B, dbc, box) ||
+        !make_map4(&tmC, p.C, dbc, box) || !make_map4(&tmY, p.y, dx, box))
+        return cudaErrorInvalidValue;
+
+    if (a.varlen) {
+        k_fused_varlen_setup<<<1, 1024, 0, p.stream>>>(a, p.P, p.N);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    e = cudaFuncSetAttribute(k_ssd_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    k_ssd_fused<<<w.grid, kThreads, kSmemBytes, p.stream>>>(tmX, tmB, tmC, tmY, a);
+    return cudaGetLastError();
+}
+
+}  // namespace ssd

@@ -42,7 +42,12 @@ size_t tc_workspace_bytes(const Problem &p);
 int tc_supported(const Problem &p);
 cudaError_t tc_launch(const Problem &p);
 
-// ---- shared helpers (ssd_common.cu) ----
+// ---- fused single-pass tensor-core path (ssd_fused.cu) ----
+size_t fused_workspace_bytes(const Problem &p);
+int fused_supported(const Problem &p);
+cudaError_t fused_launch(const Problem &p);
+
+// ---- shared helpers (ssd_api.cu) ----
 // Device check of cu_seqlens: cu[0]==0, cu[nseq]==seqlen, non-decreasing.
 // Sets *status = SSD_ERR_DEVICE_INPUT when malformed.
 cudaError_t launch_validate_cu(const Problem &p);

@@ -1,4 +1,4 @@
-// Allocation-free variant of the tensor-core SSD scan.
+// Allocation-free variant of the two-pass tensor-core SSD scan.
 //
 // Some callers cannot allocate device memory at the time they run the scan:
 // code that executes inside another framework's execution hook (an inference
@@ -6,14 +6,15 @@
 // every device allocation, or a real-time loop that forbids allocation after
 // start-up.  Such callers also cannot hand ssd_scan() a workspace of the
 // size it asks for.  ssd_scan_noalloc() therefore takes only the inputs and
-// outputs and runs the tensor-core path on scratch memory that belongs to
+// outputs and runs the two-pass tensor-core kernels on scratch memory that
+// belongs to
 // this library: a fixed-size static device array, set aside on every GPU
 // that loads the library and kept until the process exits.
 //
 // Limits and rules (also stated in include/ssd.h):
 //   * the scratch holds at most kNoAllocScratchBytes; shapes that need more
 //     are rejected with SSD_ERR_WORKSPACE before anything is enqueued;
-//   * only shapes the tensor-core path takes are accepted (bf16, headdim
+//   * only shapes the two-pass kernels take are accepted (bf16, headdim
 //     64, dstate 128/256, chunk 128/256, no packed sequences);
 //   * every call uses the same array, so calls whose GPU work overlaps
 //     (different streams, or different host threads) race with each other;

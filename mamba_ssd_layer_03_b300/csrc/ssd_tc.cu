@@ -345,12 +345,20 @@ k_chunk_state(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ C
                 tmem_ld32(t_s + mt * ncols + (hh < a.kh ? hh : 0) * 64 + p0 + lane_off, sv);
                 tmem_ld_wait();
                 if (!hok) continue;
+                // all 32 loads first: the ring slots are not known not to
+                // alias, so interleaving them with the stores would serialise
+                // one L2 round trip per element
+                float ev[32];
 #pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     const int64_t idx = (int64_t)(p0 + q) * a.N + n;
-                    float e;
-                    if (T.c == 0) e = Einit ? __ldg(Einit + idx) : 0.f;
-                    else e = __ldcg(Ein + idx);
+                    if (T.c == 0) ev[q] = Einit ? __ldg(Einit + idx) : 0.f;
+                    else ev[q] = __ldcg(Ein + idx);
+                }
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const int64_t idx = (int64_t)(p0 + q) * a.N + n;
+                    const float e = ev[q];
                     const float en = decay * e + __uint_as_float(sv[q]);
                     __stcg(Eout + idx, en);
                     eb[idx] = __float2bfloat16_rn(e);

@@ -12,12 +12,14 @@ from parity_util import (TOL, oracle_full, oracle_unit, rel_err, run_gpu, sample
 pytestmark = pytest.mark.gpu
 
 W = ssd_synth.WORKLOADS
-ALGOS = ["simt", "tc"]
+ALGOS = ["simt", "tc", "tc2"]
 
 
 def _algo_ok(inp, algo, chunk=None):
-    """Whether `algo` takes this input (the tensor-core path is bf16 only,
-    headdim 64, dstate 128/256, chunk 128/256, no packed sequences)."""
+    """Whether `algo` takes this input: "tc" is the fused tensor-core kernel
+    (bf16, headdim 64, dstate 128, any chunk size, packed sequences too) or,
+    for other tensor-core shapes, the two-pass kernels; "tc2" is the two-pass
+    kernels (bf16, headdim 64, dstate 128/256, chunk 128/256, no packing)."""
     if algo == "simt":
         return True
     import mamba_ssd_layer_03_b300 as ssd
@@ -26,12 +28,12 @@ def _algo_ok(inp, algo, chunk=None):
                            inp["dstate"], inp["ngroups"], chunk or inp["chunk"], inp["nseq"], dt,
                            algo)
     try:
-        ssd.workspace_size(shape)
+        resolved = ssd.resolve_algo(shape)
     except ssd.SsdError as e:
         if e.code == 2:
             return False
         raise
-    return inp["cu_seqlens"] is None
+    return resolved == "tc" or inp["cu_seqlens"] is None
 
 
 def _compare_full(inp, algo, chunk=None, D=True, init=True):
@@ -109,6 +111,19 @@ def test_short_and_boundary_lengths_tc_chunks(chunk, L):
     inp = ssd_synth.make_inputs(W[1], seed=1000 + L, batch=2, seqlen=L, nheads=4, init_states=True)
     for algo in ALGOS:
         _compare_full(inp, algo, chunk=chunk)
+
+
+@pytest.mark.parametrize("segs", [None, [130, 1, 600, 257, 512, 12]])
+def test_lanes_split_between_ctas(segs):
+    """More (sequence, head pair) lanes than SMs, so that the fused kernel
+    hands the running state of a lane from one CTA to the next."""
+    if segs is None:
+        inp = ssd_synth.make_inputs(W[1], seed=31, batch=2, seqlen=300, nheads=160,
+                                    init_states=True)
+    else:
+        inp = ssd_synth.make_inputs(W[4], seed=32, seqlen=sum(segs), nheads=64,
+                                    init_states=True, segment_lengths=segs)
+    _compare_full(inp, "tc")
 
 
 @pytest.mark.parametrize("algo", ALGOS)

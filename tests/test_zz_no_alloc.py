@@ -37,8 +37,9 @@ def test_noalloc_matches_workspace_entry_point_twice():
     w = ssd_synth.WORKLOADS[1]
     inp = ssd_synth.make_inputs(w, seed=21, batch=2, seqlen=1000, nheads=6, init_states=True)
     d = _dev(inp)
+    # the allocation-free entry point runs the two-pass tensor-core kernels
     y_ref, f_ref = ssd.ssd_scan(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], w.chunk,
-                                d["initial_states"], None, True, "tc", check_status=True)
+                                d["initial_states"], None, True, "tc2", check_status=True)
     torch.cuda.synchronize()
     shape = ssd.make_shape(inp["batch"], inp["seqlen"], inp["nheads"], inp["headdim"],
                            inp["dstate"], inp["ngroups"], w.chunk, inp["nseq"], torch.bfloat16, "tc")
@@ -60,9 +61,11 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     lib = ssd.load_library()
     # The 2.7B-shaped layer needs far more than the fixed scratch holds.
     w = ssd_synth.WORKLOADS[2]
+    need = ssd.make_shape(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk,
+                          w.batch, torch.bfloat16, "tc2")
+    assert ssd.workspace_size(need) > (32 << 20)
     shape = ssd.make_shape(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk,
                            w.batch, torch.bfloat16, "tc")
-    assert ssd.workspace_size(shape) > (32 << 20)
     fake = ctypes.c_void_p(1 << 20)   # never dereferenced: the size check comes first
     rc = lib.ssd_scan_noalloc(ctypes.byref(shape), fake, fake, fake, fake, fake, None, None, fake,
                               None, None, None)
