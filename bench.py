@@ -162,6 +162,48 @@ class ClockSampler:
                 "source": self.source}
 
 
+KERNEL_OF_ALGO = {"tc": ("k_ssd_fused", "ssd_fused.cu"),
+                  "tc2": ("k_chunk_state + k_chunk_output", "ssd_tc.cu"),
+                  "simt": ("k1..k5 SIMT kernels", "ssd_simt.cu")}
+
+
+def profiled_traffic(kernel_src: str, workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary (profiles/<kernel>_<workload>.md), or None when there is none or
+    the kernel's source has changed since the counters were taken."""
+    import hashlib
+    src = os.path.join(ROOT, "mamba_ssd_layer_03_b300", "csrc", kernel_src)
+    path = os.path.join(ROOT, "profiles", f"{kernel_src.split('.')[0]}_{workload}.md")
+    try:
+        with open(src, "rb") as f:
+            sha = hashlib.sha1(f.read()).hexdigest()
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and line.startswith("- "):
+                    k, v = line[2:].split(":", 1)
+                    fields[k.strip()] = v.strip().strip("`")
+        if fields.get("source_sha1") != sha:
+            return None
+        return int(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def aggregate_over_ranks(local_ms: float, tokens_per_rank: int, steps: int, dist=None,
+                         device=None):
+    """Whole-job throughput of `steps` timed steps: every rank processed
+    `tokens_per_rank` tokens per step; the job took as long as its slowest
+    rank.  Returns (max over ranks of the timed milliseconds, tokens/s)."""
+    world = 1
+    if dist is not None and dist.is_initialized():
+        world = dist.get_world_size()
+        t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        local_ms = float(t.item())
+    return local_ms, tokens_per_rank * world * steps / (local_ms / 1e3)
+
+
 def time_oracle_sample(inp, budget_s: float):
     """Run the CPU oracle on (sequence, head) units of ``inp`` for about
     ``budget_s`` seconds, one unit per host thread at a time; return
@@ -202,6 +244,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seqlen", type=int, default=None,
+                    help="override the workload's tokens per sequence (profiling captures)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -221,7 +265,7 @@ def main():
 
     import mamba_ssd_layer_03_b300 as ssd
 
-    inp = ssd_synth.make_inputs(w, seed=rank)
+    inp = ssd_synth.make_inputs(w, seed=rank, seqlen=args.seqlen)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     shape = ssd.make_shape(inp["batch"], inp["seqlen"], inp["nheads"], inp["headdim"],
                            inp["dstate"], inp["ngroups"], inp["chunk"], inp["nseq"],
@@ -274,13 +318,9 @@ def main():
         time.sleep(0.15)
     total_ms = ev0.elapsed_time(ev1)
     per_step = [a.elapsed_time(b) for a, b in step_ev]
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
     tokens = inp["batch"] * inp["seqlen"]
-    value = tokens * world * args.steps / (total_ms / 1e3)
+    total_ms, value = aggregate_over_ranks(total_ms, tokens, args.steps, dist, dev)
+    ms_per_step = total_ms / args.steps
     kernel_ms = statistics.mean(per_step)
     achieved_gbs = nbytes / (kernel_ms / 1e3) / 1e9
     tflops = causal / (ms_per_step / 1e3) / 1e12
@@ -349,14 +389,18 @@ def main():
             "roofline_time_ms": t_roof_ms, "frac_of_roofline": t_roof_ms / ms_per_step,
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
-                         "traffic": None, "peak_source": peaks["source"],
-                         "kernel": "whole ssd_scan step (all launches)",
+                         "traffic": profiled_traffic(KERNEL_OF_ALGO[algo][1], w.name)
+                         if args.seqlen is None else None,
+                         "peak_source": peaks["source"],
+                         "kernel": KERNEL_OF_ALGO[algo][0] + " (timed as the whole ssd_scan call)",
                          "algorithmic_bytes": nbytes, "kernel_ms": kernel_ms},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": None,
             "clocks": clocks,
         }
+        if args.seqlen is not None:
+            out["config"]["seqlen_override"] = args.seqlen
         out["gpu_launches"] = launches_per_step(algo, inp) * args.steps
         print(json.dumps(out))
     if dist:
@@ -369,7 +413,9 @@ def launches_per_step(algo, inp):
     varlen = inp["cu_seqlens"] is not None
     if algo == "simt":
         return 4 + (2 if varlen else 0)
-    return 1 + (1 if varlen else 0)
+    if algo == "tc":       # fused kernel (+ cu_seqlens check and set-up)
+        return 1 + (2 if varlen else 0)
+    return 2
 
 
 def run_reference(args, w, rank, world):
