@@ -274,14 +274,51 @@ __device__ __forceinline__ uint32_t m_col(int kk, int hh) {
     return (uint32_t)(32 * (kk >> 1) + 16 * hh + 8 * (kk & 1));
 }
 
-__device__ __forceinline__ uint4 scale_bf16x8(uint4 u, float s) {
-    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
+
+
+// Masked block, one 32-column chunk holding the row's own token, with one
+// exponential per element (taken only when the chunk's total decay is too
+// large for the factored form).  Reads the C B^T chunk at `taddr` and writes
+// both heads' bf16 pieces over it.  All 32 lanes of the warp call it.
+__device__ __noinline__ void mask_chunk_exact(uint32_t taddr, float cs0, float cs1,
+                                              const float *cj0, const float *cj1,
+                                              const float *dj0, const float *dj1, int lim,
+                                              float dd0, float dd1) {
+    uint32_t v[32];
+    tmem_ld32(taddr, v);
+    tmem_ld_wait();
+    uint32_t pk0[16], pk1[16];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float2 f = bf2_to_f2(w[q]);
-        w[q] = pack_bf16x2(f.x * s, f.y * s);
+    for (int q = 0; q < 16; ++q) {
+        const int j0 = 2 * q, j1 = 2 * q + 1;
+        const float c0 = __uint_as_float(v[j0]), c1 = __uint_as_float(v[j1]);
+        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+        if (j0 <= lim) {
+            a0 = c0 * __expf(cs0 - cj0[j0]) * dj0[j0];
+            b0 = c0 * __expf(cs1 - cj1[j0]) * dj1[j0];
+        }
+        if (j1 <= lim) {
+            a1 = c1 * __expf(cs0 - cj0[j1]) * dj0[j1];
+            b1 = c1 * __expf(cs1 - cj1[j1]) * dj1[j1];
+        }
+        if (j0 == lim) { a0 += dd0; b0 += dd1; }
+        if (j1 == lim) { a1 += dd0; b1 += dd1; }
+        pk0[q] = pack_bf16x2(a0, a1);
+        pk1[q] = pack_bf16x2(b0, b1);
     }
-    return make_uint4(w[0], w[1], w[2], w[3]);
+    tmem_st16(taddr, pk0);
+    tmem_st16(taddr + 16, pk1);
 }
 
 // ----------------------------------------------------------------------------
@@ -461,81 +498,36 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         int prev_mode = 0, prev_head = 0, prev_tok = 0, prev_row = 0;
         int64_t prev_y = -1;
         bool pend_store = false;   // a TMA store of y still reads this half of Xw
-        // y of block kk: acc (TMEM) -> bf16 -> this head's half of the Xw
-        // buffer (free once the S product of the following block has read
-        // it; the caller has waited for that) -> TMA store.
-        auto epilogue = [&](uint32_t kk) {
-            const int ps = kk & 1;
-            fwait(&sm->mx_done[ps], (kk >> 1) & 1, a.status);
-            tc_fence_after();
-            const uint32_t R_prev = tbase + 256 + 128 * ps;
-            uint8_t *stile = sXw + (size_t)h * kT16;
-            uint8_t *srow = stile + t * 128;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t v[32];
-                tmem_ld32(R_prev + lane_off + h * 64 + half * 32, v);
-                tmem_ld_wait();
-                uint4 pk[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    pk[c] = make_uint4(
-                        pack_bf16x2(__uint_as_float(v[8 * c]), __uint_as_float(v[8 * c + 1])),
-                        pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3])),
-                        pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5])),
-                        pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])));
-                if (prev_mode == 1) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        *(uint4 *)(srow + (((half * 4 + c) ^ (t & 7)) << 4)) = pk[c];
-                } else if (prev_mode == 2 && prev_y >= 0) {
-                    uint4 *dst = (uint4 *)(a.y + prev_y + half * 32);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) dst[c] = pk[c];
+
+        for (uint32_t k = 0;; ++k) {
+            const bool have = w.valid;
+            if (have) {
+                const Lane &ln = w.ln;
+                const bool hv = h < ln.nh;
+                const int head = ln.h0 + (hv ? h : 0);
+                const int slot = k & 1;
+                const uint32_t R_acc = tbase + 256 + 128 * slot;
+                const bool seg_start = w.b == w.b_begin;
+                if (seg_start) {
+                    Ah = hv ? __ldg(a.A + head) : 0.f;
+                    D0 = a.D ? __ldg(a.D + ln.h0) : 0.f;
+                    D1 = (a.D && ln.nh > 1) ? __ldg(a.D + ln.h0 + 1) : 0.f;
                 }
-            }
-            tc_fence_before();
-            mbar_arrive(&sm->acc_free[ps]);
-            if (prev_mode == 1) fence_proxy_async_smem();
-            named_bar(bar_wg, 128);
-            if (t == 0 && prev_mode == 1) {
-                tma_store_4d(&tmY, stile, 0, prev_head, prev_tok, prev_row);
-                tma_store_commit();
-                pend_store = true;
-            }
-        };
 
-        uint32_t k = 0;
-        for (; w.valid; walk_next(a, w), ++k) {
-            const Lane &ln = w.ln;
-            const bool hv = h < ln.nh;
-            const int head = ln.h0 + (hv ? h : 0);
-            const int slot = k & 1;
-            const uint32_t R_acc = tbase + 256 + 128 * slot;
-            const int i0 = w.b * kB;
-            const bool tv = hv && (i0 + t < ln.len);
-            const bool seg_start = w.b == w.b_begin;
-            if (seg_start) {
-                Ah = hv ? __ldg(a.A + head) : 0.f;
-                D0 = a.D ? __ldg(a.D + ln.h0) : 0.f;
-                D1 = (a.D && ln.nh > 1) ? __ldg(a.D + ln.h0 + 1) : 0.f;
-            }
-
-            // (a) dt and the within-block cumulative decay cs of head h
-            if (!have_next) prefetch_dt(ln, w.b, slot);
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            const float d = sm->dtn[slot][h][t];
-            have_next = w.b + 1 < w.b_end;
-            if (have_next) prefetch_dt(ln, w.b + 1, slot ^ 1);
-            float incl = d * Ah;
+                // (a) dt and the within-block cumulative decay cs of head h
+                if (!have_next) prefetch_dt(ln, w.b, slot);
+                asm volatile("cp.async.wait_all;" ::: "memory");
+                const float d = sm->dtn[slot][h][t];
+                have_next = w.b + 1 < w.b_end;
+                if (have_next) prefetch_dt(ln, w.b + 1, slot ^ 1);
+                float incl = d * Ah;
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float v = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += v;
-            }
-            if (lane == 31) sm->part[h][wq] = incl;
-            named_bar(bar_wg, 128);
-            {
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float v = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += v;
+                }
+                if (lane == 31) sm->part[h][wq] = incl;
+                named_bar(bar_wg, 128);
                 const float p0 = sm->part[h][0], p1 = sm->part[h][1], p2 = sm->part[h][2],
                             p3 = sm->part[h][3];
                 incl += (wq > 0 ? p0 : 0.f) + (wq > 1 ? p1 : 0.f) + (wq > 2 ? p2 : 0.f);
@@ -544,17 +536,17 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 sm->cs[slot][h][t] = incl;
                 sm->dtv[slot][h][t] = d;
                 sm->vf[slot][h][t] = __expf(sub_end - incl) * d;
-                // reuse part[] only after every thread has read it
                 const float w_t = __expf(fminf(cs_last - incl, 0.f)) * d;
                 const float decay = __expf(cs_last);
 
-                // (d) H_k -> H_op (bf16, operand of C H^T) and H <- decay H_k
-                //     in TMEM, ready for the S product to accumulate on
-                const float *init_src = nullptr;
-                bool from_slot = false;
+                // (d) H_k -> H_op (bf16, operand of C H^T) and H <- decay H_k in
+                //     TMEM, ready for the S product to accumulate on.  A lane's
+                //     first block takes H_k from the initial state (or the
+                //     previous CTA's handoff) through TMEM.
                 if (seg_start) {
+                    const float *src = nullptr;
+                    bool from_slot = false;
                     if (w.b_begin > 0) {
-                        // state at the split point, handed over by the previous ticket
                         const int *flag = a.hflag + (ticket - 1);
                         const uint64_t tw = globaltimer_ns();
                         while (ld_acquire_i(flag) == 0) {
@@ -565,35 +557,37 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                             }
                             __nanosleep(64);
                         }
-                        init_src = a.hslot + (size_t)(ticket - 1) * kStateFloats + h * kP * kN;
+                        src = a.hslot + (size_t)(ticket - 1) * kStateFloats + h * kP * kN;
                         from_slot = true;
                     } else if (a.init && hv) {
-                        init_src = a.init + ((int64_t)ln.s * a.H + head) * kP * kN;
+                        src = a.init + ((int64_t)ln.s * a.H + head) * kP * kN;
                     }
+                    if (!hv) src = nullptr;
+#pragma unroll 1
+                    for (int c4 = 0; c4 < kP / 4; ++c4) {
+                        uint32_t r[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            float e = 0.f;
+                            if (src) {
+                                const float *sp = src + (c4 * 4 + q) * kN + t;
+                                e = from_slot ? __ldcg(sp) : __ldg(sp);
+                            }
+                            r[q] = __float_as_uint(e);
+                        }
+                        tmem_st4(R_H + lane_off + h * 64 + c4 * 4, r);
+                    }
+                    tmem_st_wait();
                 } else {
                     fwait(&sm->s_done, (k - 1) & 1, a.status);
                     tc_fence_after();
                 }
-                uint8_t *hrow = sH + h * kT16 + t * 128;
                 {
+                    uint8_t *hrow = sH + h * kT16 + t * 128;
                     uint32_t v[2][32];
-                    if (seg_start) {
-#pragma unroll
-                        for (int half = 0; half < 2; ++half)
-#pragma unroll
-                            for (int q = 0; q < 32; ++q) {
-                                float e = 0.f;
-                                if (hv && init_src) {
-                                    const float *src = init_src + (half * 32 + q) * kN + t;
-                                    e = from_slot ? __ldcg(src) : __ldg(src);
-                                }
-                                v[half][q] = __float_as_uint(e);
-                            }
-                    } else {
-                        tmem_ld32(R_H + lane_off + h * 64, v[0]);
-                        tmem_ld32(R_H + lane_off + h * 64 + 32, v[1]);
-                        tmem_ld_wait();
-                    }
+                    tmem_ld32(R_H + lane_off + h * 64, v[0]);
+                    tmem_ld32(R_H + lane_off + h * 64 + 32, v[1]);
+                    tmem_ld_wait();
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -626,105 +620,86 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         const int pc = c ^ (t & 7);
-                        dst[pc] = scale_bf16x8(src[pc], w_t);
+                        const uint4 u = src[pc];
+                        uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 f = bf2_to_f2(ww[q]);
+                            ww[q] = pack_bf16x2(f.x * w_t, f.y * w_t);
+                        }
+                        dst[pc] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
                     }
                 }
                 tmem_st_wait();
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(&sm->xw_ready);
-            }
 
-            // (e) masked block, in place over C B^T: this warpgroup turns
-            //     columns j in [64 h, 64 h + 64) into both heads' M pieces;
-            //     then acc_h *= exp(cs_h[i]) for head h
-            fwait(&sm->cb_done, k & 1, a.status);
-            named_bar(3, 256);        // cs, dtv, vf of both heads are visible
-            tc_fence_after();
-            {
-                const int i = t;
-                const int ib = wq;
-                const float(*cs)[kB] = sm->cs[slot];
-                const float(*vfs)[kB] = sm->vf[slot];
-                const float(*dts)[kB] = sm->dtv[slot];
-                const float cs0 = cs[0][i], cs1 = cs[1][i];
+                // (e) masked block, in place over C B^T: this warpgroup turns
+                //     columns j in [64 h, 64 h + 64) into both heads' M pieces;
+                //     then acc_h *= exp(cs_h[i]) for head h
+                fwait(&sm->cb_done, k & 1, a.status);
+                named_bar(3, 256);        // cs, dtv, vf of both heads are visible
+                tc_fence_after();
+                {
+                    const int i = t;
+                    const int ib = wq;
+                    const float(*cs)[kB] = sm->cs[slot];
+                    const float(*vfs)[kB] = sm->vf[slot];
+                    const float(*dts)[kB] = sm->dtv[slot];
+                    const float cs0 = cs[0][i], cs1 = cs[1][i];
 #pragma unroll 1
-                for (int mm = 0; mm < 2; ++mm) {
-                    const int m = 2 * h + mm;
-                    uint32_t pk0[16], pk1[16];
-                    if (m > ib) {
+                    for (int mm = 0; mm < 2; ++mm) {
+                        const int m = 2 * h + mm;
+                        uint32_t pk0[16], pk1[16];
+                        if (m > ib) {
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) { pk0[q] = 0u; pk1[q] = 0u; }
-                    } else {
-                        uint32_t v[32];
-                        tmem_ld32(R_cb + lane_off + m * 32, v);
-                        tmem_ld_wait();
-                        if (m < ib) {
-                            const float u0 = __expf(cs0 - cs[0][m * 32 + 31]);
-                            const float u1 = __expf(cs1 - cs[1][m * 32 + 31]);
-                            const float *vf0 = vfs[0] + m * 32, *vf1 = vfs[1] + m * 32;
-#pragma unroll
-                            for (int q = 0; q < 16; ++q) {
-                                const float c0 = __uint_as_float(v[2 * q]), c1 = __uint_as_float(v[2 * q + 1]);
-                                pk0[q] = pack_bf16x2(c0 * u0 * vf0[2 * q], c1 * u0 * vf0[2 * q + 1]);
-                                pk1[q] = pack_bf16x2(c0 * u1 * vf1[2 * q], c1 * u1 * vf1[2 * q + 1]);
-                            }
+                            for (int q = 0; q < 16; ++q) { pk0[q] = 0u; pk1[q] = 0u; }
                         } else {
-                            // sub-block holding i: j <= i.  While the sub-block's
-                            // total decay R = cs[start] - cs[end] stays below 80,
-                            // exp(cs_i - cs_j) = exp(cs_i - cs_end) exp(cs_end - cs_j)
-                            // with the first factor in [1, e^R] and the second
-                            // (inside vf) in [e^-R, 1]: no overflow and no
-                            // subnormal.  Otherwise one exponential per element.
-                            const int li = i & 31;
+                            uint32_t v[32];
                             const float *cj0 = cs[0] + m * 32, *cj1 = cs[1] + m * 32;
+                            const float end0 = cj0[31], end1 = cj1[31];
+                            // Sub-blocks before i's: j <= i for all of them;
+                            // exp(cs_i - cs_j) = exp(cs_i - cs_end) exp(cs_end - cs_j),
+                            // both factors <= 1.  i's own sub-block: the same
+                            // factors, the first in [1, e^R] and the second in
+                            // [e^-R, 1] with R the sub-block's total decay, used
+                            // while R < 80; otherwise one exponential per element.
+                            const bool own = (m == ib);
+                            const int lim = own ? (i & 31) : 31;
                             const float ref0 = (m == 0) ? 0.f : cs[0][m * 32 - 1];
                             const float ref1 = (m == 0) ? 0.f : cs[1][m * 32 - 1];
-                            const bool fast = (ref0 - cj0[31] < 80.f) && (ref1 - cj1[31] < 80.f);
+                            const bool fast = !own || ((ref0 - end0 < 80.f) && (ref1 - end1 < 80.f));
+                            const float dd0 = own ? D0 : 0.f, dd1 = own ? D1 : 0.f;
                             if (fast) {
-                                const float u0 = __expf(cs0 - cj0[31]);
-                                const float u1 = __expf(cs1 - cj1[31]);
+                                tmem_ld32(R_cb + lane_off + m * 32, v);
+                                tmem_ld_wait();
+                                const float u0 = __expf(cs0 - end0), u1 = __expf(cs1 - end1);
                                 const float *vf0 = vfs[0] + m * 32, *vf1 = vfs[1] + m * 32;
 #pragma unroll
                                 for (int q = 0; q < 16; ++q) {
                                     const int j0 = 2 * q, j1 = 2 * q + 1;
-                                    const float c0 = (j0 <= li) ? __uint_as_float(v[j0]) : 0.f;
-                                    const float c1 = (j1 <= li) ? __uint_as_float(v[j1]) : 0.f;
-                                    float a0 = c0 * u0 * vf0[j0], a1 = c1 * u0 * vf0[j1];
-                                    float b0 = c0 * u1 * vf1[j0], b1 = c1 * u1 * vf1[j1];
-                                    if (j0 == li) { a0 += D0; b0 += D1; }
-                                    if (j1 == li) { a1 += D0; b1 += D1; }
+                                    const float c0 = (j0 <= lim) ? __uint_as_float(v[j0]) : 0.f;
+                                    const float c1 = (j1 <= lim) ? __uint_as_float(v[j1]) : 0.f;
+                                    const float2 f0 = *(const float2 *)(vf0 + j0);
+                                    const float2 f1 = *(const float2 *)(vf1 + j0);
+                                    float a0 = c0 * u0 * f0.x, a1 = c1 * u0 * f0.y;
+                                    float b0 = c0 * u1 * f1.x, b1 = c1 * u1 * f1.y;
+                                    if (j0 == lim && own) { a0 += dd0; b0 += dd1; }
+                                    if (j1 == lim && own) { a1 += dd0; b1 += dd1; }
                                     pk0[q] = pack_bf16x2(a0, a1);
                                     pk1[q] = pack_bf16x2(b0, b1);
                                 }
                             } else {
-                                const float *dj0 = dts[0] + m * 32, *dj1 = dts[1] + m * 32;
-#pragma unroll
-                                for (int q = 0; q < 16; ++q) {
-                                    const int j0 = 2 * q, j1 = 2 * q + 1;
-                                    const float c0 = __uint_as_float(v[j0]), c1 = __uint_as_float(v[j1]);
-                                    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-                                    if (j0 <= li) {
-                                        a0 = c0 * __expf(cs0 - cj0[j0]) * dj0[j0];
-                                        b0 = c0 * __expf(cs1 - cj1[j0]) * dj1[j0];
-                                    }
-                                    if (j1 <= li) {
-                                        a1 = c1 * __expf(cs0 - cj0[j1]) * dj0[j1];
-                                        b1 = c1 * __expf(cs1 - cj1[j1]) * dj1[j1];
-                                    }
-                                    if (j0 == li) { a0 += D0; b0 += D1; }
-                                    if (j1 == li) { a1 += D0; b1 += D1; }
-                                    pk0[q] = pack_bf16x2(a0, a1);
-                                    pk1[q] = pack_bf16x2(b0, b1);
-                                }
+                                mask_chunk_exact(R_cb + lane_off + m * 32, cs0, cs1, cj0, cj1,
+                                                 dts[0] + m * 32, dts[1] + m * 32, lim, dd0, dd1);
+                                continue;
                             }
                         }
+                        tmem_st16(R_cb + lane_off + m * 32, pk0);
+                        tmem_st16(R_cb + lane_off + m * 32 + 16, pk1);
                     }
-                    tmem_st16(R_cb + lane_off + m * 32, pk0);
-                    tmem_st16(R_cb + lane_off + m * 32 + 16, pk1);
-                }
-                const float e = __expf(h == 0 ? cs0 : cs1);
-                {
+                    const float e = __expf(h == 0 ? cs0 : cs1);
                     uint32_t v[32], u[32];
                     tmem_ld32(R_acc + lane_off + h * 64, v);
                     tmem_ld32(R_acc + lane_off + h * 64 + 32, u);
@@ -736,19 +711,70 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     }
                     tmem_st32(R_acc + lane_off + h * 64, v);
                     tmem_st32(R_acc + lane_off + h * 64 + 32, u);
+                    tmem_st_wait();
                 }
-                tmem_st_wait();
-            }
-            tc_fence_before();
-            mbar_arrive(&sm->m_ready);
+                tc_fence_before();
+                mbar_arrive(&sm->m_ready);
 
-            // (c) epilogue of the previous block, staged in Xw once the S
-            //     product of this block has read it
-            fwait(&sm->s_done, k & 1, a.status);
-            tc_fence_after();
-            if (k >= 1) epilogue(k - 1);
+                // the S product of this block has read Xw once s_done completes
+                fwait(&sm->s_done, k & 1, a.status);
+                tc_fence_after();
+            } else if (k >= 1) {
+                // after the last block: the last y store has read its half of Xw
+                if (t == 0 && pend_store) tma_store_wait_read0();
+                named_bar(bar_wg, 128);
+            }
+
+            // (c) epilogue of the previous block: acc (TMEM) -> bf16 -> this
+            //     head's half of Xw -> TMA store
+            if (k >= 1) {
+                const uint32_t kk = k - 1;
+                const int ps = kk & 1;
+                fwait(&sm->mx_done[ps], (kk >> 1) & 1, a.status);
+                tc_fence_after();
+                const uint32_t R_prev = tbase + 256 + 128 * ps;
+                uint8_t *stile = sXw + (size_t)h * kT16;
+                uint8_t *srow = stile + t * 128;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v[32];
+                    tmem_ld32(R_prev + lane_off + h * 64 + half * 32, v);
+                    tmem_ld_wait();
+                    uint4 pk[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        pk[c] = make_uint4(
+                            pack_bf16x2(__uint_as_float(v[8 * c]), __uint_as_float(v[8 * c + 1])),
+                            pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3])),
+                            pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5])),
+                            pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])));
+                    if (prev_mode == 1) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            *(uint4 *)(srow + (((half * 4 + c) ^ (t & 7)) << 4)) = pk[c];
+                    } else if (prev_mode == 2 && prev_y >= 0) {
+                        uint4 *dst = (uint4 *)(a.y + prev_y + half * 32);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) dst[c] = pk[c];
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&sm->acc_free[ps]);
+                if (prev_mode == 1) fence_proxy_async_smem();
+                named_bar(bar_wg, 128);
+                if (t == 0 && prev_mode == 1) {
+                    tma_store_4d(&tmY, stile, 0, prev_head, prev_tok, prev_row);
+                    tma_store_commit();
+                    pend_store = true;
+                }
+            }
+            if (!have) break;
 
             // end of this CTA's part of the lane: the state after the block
+            const Lane &ln = w.ln;
+            const bool hv = h < ln.nh;
+            const int head = ln.h0 + (hv ? h : 0);
+            const int i0 = w.b * kB;
             if (w.b + 1 == w.b_end) {
                 const bool fin = w.b_end == ln.nb;
                 float *dst = nullptr;
@@ -758,14 +784,15 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 } else {
                     dst = a.hslot + (size_t)ticket * kStateFloats + h * kP * kN;
                 }
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t v[32];
-                    tmem_ld32(R_H + lane_off + h * 64 + half * 32, v);
+#pragma unroll 1
+                for (int c4 = 0; c4 < kP / 4; ++c4) {
+                    uint32_t r[4];
+                    tmem_ld4(R_H + lane_off + h * 64 + c4 * 4, r);
                     tmem_ld_wait();
                     if (dst) {
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) __stcg(dst + (half * 32 + q) * kN + t, __uint_as_float(v[q]));
+                        for (int q = 0; q < 4; ++q)
+                            __stcg(dst + (c4 * 4 + q) * kN + t, __uint_as_float(r[q]));
                     }
                 }
                 tc_fence_before();
@@ -777,20 +804,15 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 }
             }
 
-            prev_y = tv ? (((int64_t)ln.row * a.L + ln.t0 + i0 + t) * a.H + head) * kP : -1;
+            prev_y = (hv && i0 + t < ln.len)
+                         ? (((int64_t)ln.row * a.L + ln.t0 + i0 + t) * a.H + head) * kP : -1;
             prev_head = head;
             prev_tok = (int)(ln.t0 + i0);
             prev_row = ln.row;
             // rows past the sequence end may be stored by TMA only where they
             // are also past the end of the batch row (TMA drops those)
             prev_mode = !hv ? 0 : (i0 + kB <= ln.len || ln.t0 + ln.len >= a.L) ? 1 : 2;
-        }
-        // epilogue of the last block (its S product has completed: the
-        // lane's end waited for it); the y stores land before exit
-        if (k >= 1) {
-            if (t == 0 && pend_store) tma_store_wait_read0();
-            named_bar(bar_wg, 128);
-            epilogue(k - 1);
+            walk_next(a, w);
         }
         if (t == 0) tma_store_wait0();
     }
