@@ -76,6 +76,29 @@ struct FArgs {
     const int *seqblk;         // [nseq + 1] prefix of blocks per sequence (varlen)
 };
 
+// One block of a CTA's walk as the compute warps need it, written by the TMA
+// thread ahead of the block's loads.  Holding it in shared memory rather than
+// in every compute thread's registers keeps the compute warps' loop state
+// small.
+enum : int {
+    kSegStart = 1,    // first block of this CTA's part of the lane
+    kFromSlot = 2,    // ... and the lane began in an earlier CTA (state handed off)
+    kSegEnd = 4,      // last block of this CTA's part of the lane
+    kFin = 8,         // ... and the lane ends here (the sequence's final state)
+    kHasNext = 16,    // the next block belongs to the same lane
+    kTmaY = 32        // y of the block may leave as one TMA tile: the block lies
+                      // inside the sequence, or its rows past the sequence are
+                      // also past the batch row (TMA drops those)
+};
+struct BDesc {
+    int row, tok, rem;   // batch row, first token of the block in it, tokens of
+                         // the sequence from tok on (may exceed the block)
+    int h0, nh, s;       // first head, heads in the lane (1 or 2), sequence
+    int flags;
+    float A[2], D[2];    // per head of the lane (0 for a missing second head)
+};
+constexpr int kDescRing = 4;
+
 struct Smem {
     // [block parity][head][token]: the other warpgroup may still read the
     // previous block's values while this one writes the next block's
@@ -87,6 +110,8 @@ struct Smem {
     uint64_t c_full, b_full, x_full[2];
     uint64_t cb_done, s_done, mx_done[2], c_empty, b_empty, x_empty[2], mma_fin;
     uint64_t hop_ready, xw_ready, m_ready, acc_free[2];
+    uint64_t desc_full[kDescRing];
+    BDesc desc[kDescRing];
     uint32_t tmem;
     int ticket;
 };
@@ -178,6 +203,12 @@ __device__ __forceinline__ void walk_load_seg(const FArgs &a, Walk &w) {
         ++w.k;
     }
     w.valid = false;
+}
+
+// Number of blocks in the range of CTA `ticket`.
+__device__ __forceinline__ int cta_blocks(const FArgs &a, int ticket) {
+    const int64_t T = total_blocks(a);
+    return (int)((int64_t)(ticket + 1) * T / a.grid - (int64_t)ticket * T / a.grid);
 }
 
 __device__ __forceinline__ void walk_init(const FArgs &a, Walk &w, int ticket) {
@@ -349,6 +380,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         mbar_init(&sm->hop_ready, 256); mbar_init(&sm->xw_ready, 256);
         mbar_init(&sm->m_ready, 256);
         mbar_init(&sm->acc_free[0], 256); mbar_init(&sm->acc_free[1], 256);
+        for (int r = 0; r < kDescRing; ++r) mbar_init(&sm->desc_full[r], 1);
         fence_mbar_init();
         prefetch_tmap(&tmX); prefetch_tmap(&tmB); prefetch_tmap(&tmC); prefetch_tmap(&tmY);
         sm->ticket = atomicAdd(a.ticket, 1);
@@ -371,6 +403,30 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             for (; w.valid; walk_next(a, w), ++k) {
                 const int tok = (int)(w.ln.t0 + (int64_t)w.b * kB);
                 const int slot = k & 1;
+                {
+                    // slot k % 4 last described block k - 4: the compute warps
+                    // were done with it (its epilogue included) before they
+                    // made block k - 2's H operand ready, which the c_empty
+                    // completion waited for in the previous iteration follows
+                    BDesc &d = sm->desc[k % kDescRing];
+                    const Lane &ln = w.ln;
+                    const int i0 = w.b * kB;
+                    d.row = ln.row;
+                    d.tok = tok;
+                    d.rem = ln.len - i0;
+                    d.h0 = ln.h0;
+                    d.nh = ln.nh;
+                    d.s = ln.s;
+                    d.flags = (w.b == w.b_begin ? kSegStart : 0) | (w.b_begin > 0 ? kFromSlot : 0) |
+                              (w.b + 1 == w.b_end ? kSegEnd : 0) | (w.b_end == ln.nb ? kFin : 0) |
+                              (w.b + 1 < w.b_end ? kHasNext : 0) |
+                              ((i0 + kB <= ln.len || ln.t0 + ln.len >= a.L) ? kTmaY : 0);
+                    d.A[0] = __ldg(a.A + ln.h0);
+                    d.A[1] = ln.nh > 1 ? __ldg(a.A + ln.h0 + 1) : 0.f;
+                    d.D[0] = a.D ? __ldg(a.D + ln.h0) : 0.f;
+                    d.D[1] = (a.D && ln.nh > 1) ? __ldg(a.D + ln.h0 + 1) : 0.f;
+                    mbar_arrive(&sm->desc_full[k % kDescRing]);
+                }
                 if (k >= 2) fwait(&sm->x_empty[slot], ((k >> 1) + 1) & 1, a.status);
                 for (int s = 0; s < 2; ++s)
                     tma_load_4d(sX + (size_t)(slot * 2 + s) * kT16, &tmX, &sm->x_full[slot], 0,
@@ -402,10 +458,8 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             const uint32_t id_mx = idesc_bf16_f32(128, 64, 0, 1);
             const uint32_t sc = smem_u32(sC), sbb = smem_u32(sB), sxw = smem_u32(sXw),
                            sh = smem_u32(sH), sx = smem_u32(sX);
-            Walk w;
-            walk_init(a, w, ticket);
-            uint32_t k = 0;
-            for (; w.valid; walk_next(a, w), ++k) {
+            const uint32_t nblk = (uint32_t)cta_blocks(a, ticket);
+            for (uint32_t k = 0; k < nblk; ++k) {
                 const int slot = k & 1;
                 const uint32_t R_acc = tbase + 256 + 128 * slot;
                 fwait(&sm->c_full, k & 1, a.status);
@@ -472,16 +526,14 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const int bar_wg = 1 + h;
 
-        Walk w;
-        walk_init(a, w, ticket);
-        // dt of this thread's token and head in block b of lane ln, copied
-        // into dtn[par][h][t] asynchronously (cp.async: barriers do not wait
-        // for it); zero outside the sequence or the lane's heads
-        auto prefetch_dt = [&](const Lane &ln, int b, int par) {
+        // dt of this thread's token and head in the block of `dk` starting
+        // `off` tokens later, copied into dtn[par][h][t] asynchronously
+        // (cp.async: barriers do not wait for it); zero outside the sequence
+        // or the lane's heads
+        auto prefetch_dt = [&](const BDesc &dk, int off, int par) {
             float *dst = &sm->dtn[par][h][t];
-            const int i = b * kB + t;
-            if (h < ln.nh && i < ln.len) {
-                const float *src = a.dt + ((int64_t)ln.row * a.L + ln.t0 + i) * a.H + ln.h0 + h;
+            if (h < dk.nh && off + t < dk.rem) {
+                const float *src = a.dt + ((int64_t)dk.row * a.L + dk.tok + off + t) * a.H + dk.h0 + h;
                 asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)),
                              "l"(src) : "memory");
             } else {
@@ -490,37 +542,28 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             asm volatile("cp.async.commit_group;" ::: "memory");
         };
         bool have_next = false;
-        float Ah = 0.f, D0 = 0.f, D1 = 0.f;
-
-        // previous block, for the deferred epilogue: how its y leaves the chip
-        // (0: no valid head here, 1: TMA store of the whole tile, 2: direct
-        // stores of the rows inside the sequence), where, and this thread's row
-        int prev_mode = 0, prev_head = 0, prev_tok = 0, prev_row = 0;
-        int64_t prev_y = -1;
         bool pend_store = false;   // a TMA store of y still reads this half of Xw
+        const uint32_t nblk = (uint32_t)cta_blocks(a, ticket);
 
         for (uint32_t k = 0;; ++k) {
-            const bool have = w.valid;
+            const bool have = k < nblk;
             if (have) {
-                const Lane &ln = w.ln;
-                const bool hv = h < ln.nh;
-                const int head = ln.h0 + (hv ? h : 0);
+                fwait(&sm->desc_full[k % kDescRing], (k / kDescRing) & 1, a.status);
+                const BDesc &dk = sm->desc[k % kDescRing];
+                const int flags = dk.flags;
+                const bool hv = h < dk.nh;
+                const int head = dk.h0 + (hv ? h : 0);
                 const int slot = k & 1;
                 const uint32_t R_acc = tbase + 256 + 128 * slot;
-                const bool seg_start = w.b == w.b_begin;
-                if (seg_start) {
-                    Ah = hv ? __ldg(a.A + head) : 0.f;
-                    D0 = a.D ? __ldg(a.D + ln.h0) : 0.f;
-                    D1 = (a.D && ln.nh > 1) ? __ldg(a.D + ln.h0 + 1) : 0.f;
-                }
+                const bool seg_start = (flags & kSegStart) != 0;
 
                 // (a) dt and the within-block cumulative decay cs of head h
-                if (!have_next) prefetch_dt(ln, w.b, slot);
+                if (!have_next) prefetch_dt(dk, 0, slot);
                 asm volatile("cp.async.wait_all;" ::: "memory");
                 const float d = sm->dtn[slot][h][t];
-                have_next = w.b + 1 < w.b_end;
-                if (have_next) prefetch_dt(ln, w.b + 1, slot ^ 1);
-                float incl = d * Ah;
+                have_next = (flags & kHasNext) != 0;
+                if (have_next) prefetch_dt(dk, kB, slot ^ 1);
+                float incl = d * dk.A[h];
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
                     const float v = __shfl_up_sync(0xffffffffu, incl, off);
@@ -546,7 +589,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 if (seg_start) {
                     const float *src = nullptr;
                     bool from_slot = false;
-                    if (w.b_begin > 0) {
+                    if (flags & kFromSlot) {
                         const int *flag = a.hflag + (ticket - 1);
                         const uint64_t tw = globaltimer_ns();
                         while (ld_acquire_i(flag) == 0) {
@@ -560,7 +603,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                         src = a.hslot + (size_t)(ticket - 1) * kStateFloats + h * kP * kN;
                         from_slot = true;
                     } else if (a.init && hv) {
-                        src = a.init + ((int64_t)ln.s * a.H + head) * kP * kN;
+                        src = a.init + ((int64_t)dk.s * a.H + head) * kP * kN;
                     }
                     if (!hv) src = nullptr;
 #pragma unroll 1
@@ -670,7 +713,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                             const float ref0 = (m == 0) ? 0.f : cs[0][m * 32 - 1];
                             const float ref1 = (m == 0) ? 0.f : cs[1][m * 32 - 1];
                             const bool fast = !own || ((ref0 - end0 < 80.f) && (ref1 - end1 < 80.f));
-                            const float dd0 = own ? D0 : 0.f, dd1 = own ? D1 : 0.f;
+                            const float dd0 = own ? dk.D[0] : 0.f, dd1 = own ? dk.D[1] : 0.f;
                             if (fast) {
                                 tmem_ld32(R_cb + lane_off + m * 32, v);
                                 tmem_ld_wait();
@@ -733,6 +776,14 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 fwait(&sm->mx_done[ps], (kk >> 1) & 1, a.status);
                 tc_fence_after();
                 const uint32_t R_prev = tbase + 256 + 128 * ps;
+                // how y leaves the chip: 0 no valid head here, 1 TMA store of
+                // the whole tile, 2 direct stores of the rows inside the sequence
+                const BDesc &dp = sm->desc[kk % kDescRing];
+                const bool hvp = h < dp.nh;
+                const int prev_mode = !hvp ? 0 : (dp.flags & kTmaY) ? 1 : 2;
+                const int prev_head = dp.h0 + (hvp ? h : 0);
+                const int64_t prev_y =
+                    (hvp && t < dp.rem) ? (((int64_t)dp.row * a.L + dp.tok + t) * a.H + prev_head) * kP : -1;
                 uint8_t *stile = sXw + (size_t)h * kT16;
                 uint8_t *srow = stile + t * 128;
 #pragma unroll
@@ -763,7 +814,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 if (prev_mode == 1) fence_proxy_async_smem();
                 named_bar(bar_wg, 128);
                 if (t == 0 && prev_mode == 1) {
-                    tma_store_4d(&tmY, stile, 0, prev_head, prev_tok, prev_row);
+                    tma_store_4d(&tmY, stile, 0, prev_head, dp.tok, dp.row);
                     tma_store_commit();
                     pend_store = true;
                 }
@@ -771,16 +822,16 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             if (!have) break;
 
             // end of this CTA's part of the lane: the state after the block
-            const Lane &ln = w.ln;
-            const bool hv = h < ln.nh;
-            const int head = ln.h0 + (hv ? h : 0);
-            const int i0 = w.b * kB;
-            if (w.b + 1 == w.b_end) {
-                const bool fin = w.b_end == ln.nb;
+            const BDesc &dk = sm->desc[k % kDescRing];
+            const int flags = dk.flags;
+            if (flags & kSegEnd) {
+                const bool hv = h < dk.nh;
+                const int head = dk.h0 + (hv ? h : 0);
+                const bool fin = (flags & kFin) != 0;
                 float *dst = nullptr;
                 if (fin) {
                     if (a.final_states && hv)
-                        dst = a.final_states + ((int64_t)ln.s * a.H + head) * kP * kN;
+                        dst = a.final_states + ((int64_t)dk.s * a.H + head) * kP * kN;
                 } else {
                     dst = a.hslot + (size_t)ticket * kStateFloats + h * kP * kN;
                 }
@@ -803,16 +854,6 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     if (tid == 0) st_release_i(a.hflag + ticket, 1);
                 }
             }
-
-            prev_y = (hv && i0 + t < ln.len)
-                         ? (((int64_t)ln.row * a.L + ln.t0 + i0 + t) * a.H + head) * kP : -1;
-            prev_head = head;
-            prev_tok = (int)(ln.t0 + i0);
-            prev_row = ln.row;
-            // rows past the sequence end may be stored by TMA only where they
-            // are also past the end of the batch row (TMA drops those)
-            prev_mode = !hv ? 0 : (i0 + kB <= ln.len || ln.t0 + ln.len >= a.L) ? 1 : 2;
-            walk_next(a, w);
         }
         if (t == 0) tma_store_wait0();
     }
