@@ -119,6 +119,26 @@ typedef struct ssd_shape {
 } ssd_shape;
 
 /*
+ * Optional transform of the raw step sizes, applied by the kernels as they
+ * read dt (the selective SSM's Delta = softplus(parameter + s_Delta(x)):
+ * Mamba-1 walkthrough "Mamba: Linear-Time Sequence Modeling with Selective
+ * State Spaces", section 三(二) "引入选择机制到 SSM 中", where Delta passes
+ * through tau_Delta = softplus).  For token t of head h:
+ *     z  = dt[t, h] + (bias ? bias[h] : 0)
+ *     dt' = softplus ? log(1 + exp(z)) : z
+ *     dt' = min(max(dt', dt_min), dt_max)
+ * and the scan uses dt' wherever the operation above has dt.  Tokens outside
+ * every sequence are not transformed.  dt_min <= dt_max is required (use 0
+ * and INFINITY for no clamp); a NULL transform means dt is used as given.
+ */
+typedef struct ssd_dt_transform {
+    const float *bias;   /* [nheads] DEVICE pointer, nullable (0) */
+    int32_t softplus;    /* nonzero: apply softplus after the bias */
+    float dt_min;        /* clamp bounds, applied last */
+    float dt_max;
+} ssd_dt_transform;
+
+/*
  * Bytes of device workspace ssd_scan() needs for `shape` (with the algorithm
  * the shape resolves to).  Writes *bytes; returns SSD_OK or the same
  * argument/support error ssd_scan() would return for this shape.
@@ -142,6 +162,63 @@ SSD_API int ssd_scan(const ssd_shape *shape, const void *x, const float *dt,
                      const float *D, const float *initial_states,
                      const int32_t *cu_seqlens, void *y, float *final_states,
                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * ssd_scan() with the step sizes first put through `dt_transform` (nullable:
+ * then exactly ssd_scan()).  The fused tensor-core kernel applies the
+ * transform as it loads dt; the other paths run a pre-pass that writes the
+ * transformed dt into the workspace, which is why the workspace size depends
+ * on the transform: ask ssd_scan_ex_workspace_size() with the same
+ * arguments.  Errors as for ssd_scan(), plus SSD_ERR_INVALID_ARG when
+ * dt_min > dt_max.
+ */
+SSD_API int ssd_scan_ex_workspace_size(const ssd_shape *shape,
+                                       const ssd_dt_transform *dt_transform,
+                                       size_t *bytes);
+SSD_API int ssd_scan_ex(const ssd_shape *shape, const void *x, const float *dt,
+                        const ssd_dt_transform *dt_transform, const float *A,
+                        const void *B, const void *C, const float *D,
+                        const float *initial_states, const int32_t *cu_seqlens,
+                        void *y, float *final_states, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/*
+ * One decode step of `batch` independent sequences: the recurrent form of the
+ * same map, one token per sequence, with the state updated in place (the
+ * selective SSM's state cache that makes generation linear-time: Mamba-1
+ * walkthrough, sections 二(一) "从连续系统到离散建模" -- recurrent updates for
+ * inference -- and 四(五) "计算效率评估").  For every sequence b and head h
+ * (group g = h / (nheads / ngroups)):
+ *     state[b, h] <- exp(dt' A_h) state[b, h] + dt' (x[b, h] (outer) B[b, g])
+ *     y[b, h]      = state[b, h] . C[b, g] + D_h x[b, h]
+ * with dt' = dt[b, h] put through dt_transform (nullable).  Equals ssd_scan()
+ * of a one-token sequence with initial_states = final_states = state.
+ *
+ * Layouts (row-major, contiguous):
+ *   x, y     [batch][nheads][headdim]           dtype (fp32 or bf16)
+ *   dt       [batch][nheads]                    fp32
+ *   A, D     [nheads]                           fp32 (D nullable: 0)
+ *   B, C     [batch][ngroups][dstate]           dtype
+ *   state    [batch][nheads][headdim][dstate]   fp32, read and written
+ * All pointers are DEVICE pointers owned by the caller; x, B, C, dt, A, D
+ * must not overlap state or y.  Any headdim and dstate in 1..1024.  No
+ * workspace, no device-side waits: every error is found on the host and
+ * returned before anything is enqueued.  Asynchronous on `stream`.
+ */
+typedef struct ssd_step_shape {
+    int64_t batch;       /* >= 0 */
+    int32_t nheads;      /* H >= 1 */
+    int32_t headdim;     /* P, 1..1024 */
+    int32_t dstate;      /* N, 1..1024 */
+    int32_t ngroups;     /* G >= 1, divides nheads */
+    int32_t dtype;       /* ssd_dtype */
+    int32_t reserved;    /* must be 0 */
+} ssd_step_shape;
+
+SSD_API int ssd_step(const ssd_step_shape *shape, const void *x, const float *dt,
+                     const ssd_dt_transform *dt_transform, const float *A,
+                     const void *B, const void *C, const float *D, float *state,
+                     void *y, void *stream);
 
 /*
  * Synchronise `stream`, then read the status word that the last ssd_scan()

@@ -19,6 +19,14 @@ initial/final states (nseq, H, P, N) fp32, cu_seqlens (nseq+1,) int32.
 If x lives on the CPU, every input is copied to the current CUDA device
 (pinned host memory makes the copies asynchronous), the scan runs there and
 y / final_states are copied back to the host.
+
+Optional step-size transform (``dt_bias``, ``dt_softplus``, ``dt_limit``):
+dt' = clamp(softplus(dt + bias)) applied by the kernels as they read dt.
+
+    y = ssd_step(x, dt, A, B, C, D, state)
+
+is one decode step (one token per sequence; x (b, H, P), dt (b, H), B/C
+(b, G, N), state (b, H, P, N) fp32 updated in place).
 """
 from __future__ import annotations
 
@@ -44,6 +52,18 @@ class SsdShape(ctypes.Structure):
                 ("dstate", ctypes.c_int32), ("ngroups", ctypes.c_int32),
                 ("chunk_size", ctypes.c_int32), ("nseq", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("algo", ctypes.c_int32)]
+
+
+class SsdDtTransform(ctypes.Structure):
+    _fields_ = [("bias", ctypes.c_void_p), ("softplus", ctypes.c_int32),
+                ("dt_min", ctypes.c_float), ("dt_max", ctypes.c_float)]
+
+
+class SsdStepShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("nheads", ctypes.c_int32),
+                ("headdim", ctypes.c_int32), ("dstate", ctypes.c_int32),
+                ("ngroups", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class SsdError(RuntimeError):
@@ -78,6 +98,13 @@ def load_library() -> ctypes.CDLL:
     lib.ssd_resolve_algo.restype = ctypes.c_int
     lib.ssd_scan_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.ssd_scan_noalloc.restype = ctypes.c_int
+    tp = ctypes.POINTER(SsdDtTransform)
+    lib.ssd_scan_ex_workspace_size.argtypes = [sp, tp, ctypes.POINTER(sz)]
+    lib.ssd_scan_ex_workspace_size.restype = ctypes.c_int
+    lib.ssd_scan_ex.argtypes = [sp, vp, vp, tp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.ssd_scan_ex.restype = ctypes.c_int
+    lib.ssd_step.argtypes = [ctypes.POINTER(SsdStepShape), vp, vp, tp, vp, vp, vp, vp, vp, vp, vp]
+    lib.ssd_step.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -98,9 +125,22 @@ def make_shape(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, nseq
                     ALGOS[algo])
 
 
-def workspace_size(shape: SsdShape) -> int:
+def make_dt_transform(dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = False,
+                      dt_limit=None) -> Optional[SsdDtTransform]:
+    """The C struct for a step-size transform, or None when no part is asked
+    for.  dt_limit = (dt_min, dt_max); None means no clamp."""
+    if dt_bias is None and not dt_softplus and dt_limit is None:
+        return None
+    lo, hi = (0.0, float("inf")) if dt_limit is None else (float(dt_limit[0]), float(dt_limit[1]))
+    return SsdDtTransform(None if dt_bias is None else dt_bias.data_ptr(), 1 if dt_softplus else 0,
+                          lo, hi)
+
+
+def workspace_size(shape: SsdShape, dt_transform: Optional[SsdDtTransform] = None) -> int:
     n = ctypes.c_size_t(0)
-    rc = load_library().ssd_scan_workspace_size(ctypes.byref(shape), ctypes.byref(n))
+    rc = load_library().ssd_scan_ex_workspace_size(
+        ctypes.byref(shape), None if dt_transform is None else ctypes.byref(dt_transform),
+        ctypes.byref(n))
     if rc != 0:
         raise SsdError(rc, "ssd_scan_workspace_size")
     return int(n.value)
@@ -136,16 +176,20 @@ def ssd_scan(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor
              cu_seqlens: Optional[torch.Tensor] = None, return_final_states: bool = True,
              algo: str = "auto", out: Optional[torch.Tensor] = None,
              final_out: Optional[torch.Tensor] = None,
-             workspace: Optional[torch.Tensor] = None, check_status: bool = False):
+             workspace: Optional[torch.Tensor] = None, check_status: bool = False,
+             dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = False,
+             dt_limit=None):
     """Run the SSD forward scan.  Returns (y, final_states or None).
 
     ``check_status=True`` synchronises and raises if the device reported a
     malformed cu_seqlens or a timed-out wait.  ``out``/``final_out``/
     ``workspace`` let a caller reuse buffers (e.g. inside a timing loop).
+    ``dt_bias`` (H,) fp32, ``dt_softplus`` and ``dt_limit`` = (lo, hi) turn
+    on the step-size transform dt' = clamp(softplus(dt + bias)).
     """
     if x.device.type == "cpu":
         return _scan_from_host(x, dt, A, B, C, D, chunk_size, initial_states, cu_seqlens,
-                               return_final_states, algo)
+                               return_final_states, algo, dt_bias, dt_softplus, dt_limit)
     lib = load_library()
     dev = x.device
     if x.dim() != 4:
@@ -167,8 +211,11 @@ def ssd_scan(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor
         nseq = cu_seqlens.numel() - 1
     if initial_states is not None:
         _check(initial_states, "initial_states", torch.float32, (nseq, H, P, N), dev)
+    if dt_bias is not None:
+        _check(dt_bias, "dt_bias", torch.float32, (H,), dev)
+    tf = make_dt_transform(dt_bias, dt_softplus, dt_limit)
     shape = make_shape(b, L, H, P, N, G, chunk_size, nseq, x.dtype, algo)
-    nbytes = workspace_size(shape)
+    nbytes = workspace_size(shape, tf)
     if workspace is None or workspace.numel() < nbytes:
         workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
     y = out if out is not None else torch.empty_like(x)
@@ -177,10 +224,16 @@ def ssd_scan(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor
         fin = final_out if final_out is not None else torch.empty(
             (nseq, H, P, N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev).cuda_stream
-    rc = lib.ssd_scan(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
-                      _ptr(D), _ptr(initial_states), _ptr(cu_seqlens), _ptr(y), _ptr(fin),
-                      _ptr(workspace), ctypes.c_size_t(workspace.numel()),
-                      ctypes.c_void_p(stream))
+    if tf is None:
+        rc = lib.ssd_scan(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                          _ptr(D), _ptr(initial_states), _ptr(cu_seqlens), _ptr(y), _ptr(fin),
+                          _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                          ctypes.c_void_p(stream))
+    else:
+        rc = lib.ssd_scan_ex(ctypes.byref(shape), _ptr(x), _ptr(dt), ctypes.byref(tf), _ptr(A),
+                             _ptr(B), _ptr(C), _ptr(D), _ptr(initial_states), _ptr(cu_seqlens),
+                             _ptr(y), _ptr(fin), _ptr(workspace),
+                             ctypes.c_size_t(workspace.numel()), ctypes.c_void_p(stream))
     if rc != 0:
         raise SsdError(rc, "ssd_scan")
     if check_status:
@@ -210,15 +263,58 @@ def ssd_scan_noalloc(x, dt, A, B, C, D=None, chunk_size=256, initial_states=None
     return y, final_out
 
 
+def ssd_step(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+             C: torch.Tensor, D: Optional[torch.Tensor], state: torch.Tensor,
+             dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = False, dt_limit=None,
+             out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One decode step: state (b, H, P, N) fp32 is updated in place; returns
+    y (b, H, P).  x (b, H, P) and B, C (b, G, N) in fp32 or bf16, dt (b, H)."""
+    lib = load_library()
+    if x.dim() != 3 or B.dim() != 3:
+        raise ValueError("x must be (batch, nheads, headdim) and B, C (batch, ngroups, dstate)")
+    b, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("ssd_step runs on CUDA tensors")
+    _check(x, "x", x.dtype, device=dev)
+    _check(dt, "dt", torch.float32, (b, H), dev)
+    _check(A, "A", torch.float32, (H,), dev)
+    _check(B, "B", x.dtype, (b, G, N), dev)
+    _check(C, "C", x.dtype, (b, G, N), dev)
+    if D is not None:
+        _check(D, "D", torch.float32, (H,), dev)
+    _check(state, "state", torch.float32, (b, H, P, N), dev)
+    if dt_bias is not None:
+        _check(dt_bias, "dt_bias", torch.float32, (H,), dev)
+    if x.dtype == torch.float32:
+        dtype = SSD_F32
+    elif x.dtype == torch.bfloat16:
+        dtype = SSD_BF16
+    else:
+        raise TypeError(f"x/B/C dtype must be float32 or bfloat16, got {x.dtype}")
+    shape = SsdStepShape(b, H, P, N, G, dtype, 0)
+    tf = make_dt_transform(dt_bias, dt_softplus, dt_limit)
+    y = out if out is not None else torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    rc = lib.ssd_step(ctypes.byref(shape), _ptr(x), _ptr(dt),
+                      None if tf is None else ctypes.byref(tf), _ptr(A), _ptr(B), _ptr(C),
+                      _ptr(D), _ptr(state), _ptr(y), ctypes.c_void_p(stream))
+    if rc != 0:
+        raise SsdError(rc, "ssd_step")
+    return y
+
+
 def _scan_from_host(x, dt, A, B, C, D, chunk_size, initial_states, cu_seqlens,
-                    return_final_states, algo):
+                    return_final_states, algo, dt_bias=None, dt_softplus=False, dt_limit=None):
     dev = torch.device("cuda", torch.cuda.current_device())
 
     def up(t):
         return None if t is None else t.to(dev, non_blocking=True)
 
     y, fin = ssd_scan(up(x), up(dt), up(A), up(B), up(C), up(D), chunk_size,
-                      up(initial_states), up(cu_seqlens), return_final_states, algo)
+                      up(initial_states), up(cu_seqlens), return_final_states, algo,
+                      dt_bias=up(dt_bias), dt_softplus=dt_softplus, dt_limit=dt_limit)
     pin = x.is_pinned()
     y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=pin)
     y_h.copy_(y, non_blocking=pin)

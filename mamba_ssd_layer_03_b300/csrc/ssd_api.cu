@@ -60,14 +60,37 @@ size_t workspace_for(const Problem &p, int algo) {
 
 // The two-pass kernels take no packed sequences.  A shape with one batch row
 // may come with cu_seqlens, and AUTO then falls back to SIMT, so the
-// workspace asked for covers both.
-size_t workspace_need(const ssd_shape *s, const Problem &p, int algo) {
+// workspace asked for covers both.  With a step-size transform, every path
+// but the fused kernel reads the transformed dt from the end of the
+// workspace.
+size_t dt_prepass_bytes(const Problem &p) {
+    return align_up((size_t)(p.batch * p.seqlen * p.H) * sizeof(float), 256);
+}
+
+size_t workspace_need(const ssd_shape *s, const Problem &p, int algo, bool dt_tf) {
     size_t need = workspace_for(p, algo);
+    bool fallback = false;
     if (algo == SSD_ALGO_TC_TWOPASS && s->algo == SSD_ALGO_AUTO && p.batch == 1) {
         const size_t simt = workspace_for(p, SSD_ALGO_SIMT);
         if (simt > need) need = simt;
+        fallback = true;
     }
+    if (dt_tf && (algo != SSD_ALGO_TC || fallback)) need = align_up(need, 256) + dt_prepass_bytes(p);
     return need;
+}
+
+// Host check of a step-size transform; fills `t` (off for NULL).
+int resolve_dtt(const ssd_dt_transform *d, DtTransform &t) {
+    t = DtTransform();
+    if (!d) return SSD_OK;
+    if (!(d->dt_min <= d->dt_max)) return SSD_ERR_INVALID_ARG;   // also rejects NaN
+    if (d->bias && ((uintptr_t)d->bias % 4) != 0) return SSD_ERR_UNSUPPORTED;
+    t.bias = d->bias;
+    t.softplus = d->softplus != 0;
+    t.lo = d->dt_min;
+    t.hi = d->dt_max;
+    t.on = true;
+    return SSD_OK;
 }
 
 bool aligned(const void *ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
@@ -105,14 +128,22 @@ SSD_API int ssd_resolve_algo(const ssd_shape *shape) {
     return rc == SSD_OK ? algo : -rc;
 }
 
-SSD_API int ssd_scan_workspace_size(const ssd_shape *shape, size_t *bytes) {
+SSD_API int ssd_scan_ex_workspace_size(const ssd_shape *shape,
+                                       const ssd_dt_transform *dt_transform, size_t *bytes) {
     if (!bytes) return SSD_ERR_INVALID_ARG;
     Problem p;
     int algo = 0;
-    const int rc = resolve(shape, p, &algo);
+    int rc = resolve(shape, p, &algo);
     if (rc != SSD_OK) return rc;
-    *bytes = workspace_need(shape, p, algo);
+    DtTransform tf;
+    rc = resolve_dtt(dt_transform, tf);
+    if (rc != SSD_OK) return rc;
+    *bytes = workspace_need(shape, p, algo, tf.on);
     return SSD_OK;
+}
+
+SSD_API int ssd_scan_workspace_size(const ssd_shape *shape, size_t *bytes) {
+    return ssd_scan_ex_workspace_size(shape, nullptr, bytes);
 }
 
 SSD_API int ssd_scan(const ssd_shape *shape, const void *x, const float *dt, const float *A,
@@ -120,16 +151,27 @@ SSD_API int ssd_scan(const ssd_shape *shape, const void *x, const float *dt, con
                      const float *initial_states, const int32_t *cu_seqlens, void *y,
                      float *final_states, void *workspace, size_t workspace_bytes,
                      void *stream) {
+    return ssd_scan_ex(shape, x, dt, nullptr, A, B, C, D, initial_states, cu_seqlens, y,
+                       final_states, workspace, workspace_bytes, stream);
+}
+
+SSD_API int ssd_scan_ex(const ssd_shape *shape, const void *x, const float *dt,
+                        const ssd_dt_transform *dt_transform, const float *A, const void *B,
+                        const void *C, const float *D, const float *initial_states,
+                        const int32_t *cu_seqlens, void *y, float *final_states, void *workspace,
+                        size_t workspace_bytes, void *stream) {
     Problem p;
     int algo = 0;
     int rc = resolve(shape, p, &algo);
+    if (rc != SSD_OK) return rc;
+    rc = resolve_dtt(dt_transform, p.dtt);
     if (rc != SSD_OK) return rc;
     if (cu_seqlens) {
         if (p.batch != 1 || p.nseq < 1) return SSD_ERR_INVALID_ARG;
     } else if (p.nseq != p.batch) {
         return SSD_ERR_INVALID_ARG;
     }
-    const size_t need = workspace_need(shape, p, algo);
+    const size_t need = workspace_need(shape, p, algo, p.dtt.on);
     if (cu_seqlens && algo == SSD_ALGO_TC_TWOPASS) {
         if (shape->algo != SSD_ALGO_AUTO) return SSD_ERR_UNSUPPORTED;
         algo = SSD_ALGO_SIMT;
@@ -169,10 +211,45 @@ SSD_API int ssd_scan(const ssd_shape *shape, const void *x, const float *dt, con
         }
         return SSD_OK;
     }
+    if (p.dtt.on && algo != SSD_ALGO_TC) {
+        // the other paths read dt in several kernels: transform it once into
+        // the end of the workspace
+        float *dt_eff = (float *)((char *)workspace + (need - dt_prepass_bytes(p)));
+        if (launch_dt_transform(p, dt_eff) != cudaSuccess) return SSD_ERR_CUDA;
+        p.dt = dt_eff;
+        p.dtt = DtTransform();
+    }
     const cudaError_t e = (algo == SSD_ALGO_TC)          ? fused_launch(p)
                           : (algo == SSD_ALGO_TC_TWOPASS) ? tc_launch(p)
                                                           : simt_launch(p);
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+SSD_API int ssd_step(const ssd_step_shape *shape, const void *x, const float *dt,
+                     const ssd_dt_transform *dt_transform, const float *A, const void *B,
+                     const void *C, const float *D, float *state, void *y, void *stream) {
+    if (!shape) return SSD_ERR_INVALID_ARG;
+    const ssd_step_shape &s = *shape;
+    if (s.batch < 0 || s.nheads < 1 || s.headdim < 1 || s.dstate < 1 || s.ngroups < 1 ||
+        s.nheads % s.ngroups != 0 || s.reserved != 0)
+        return SSD_ERR_INVALID_ARG;
+    if (s.dtype != SSD_F32 && s.dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
+    if (s.headdim > 1024 || s.dstate > 1024) return SSD_ERR_UNSUPPORTED;
+    if (s.batch * s.nheads > (int64_t)INT32_MAX) return SSD_ERR_UNSUPPORTED;
+    StepProblem p;
+    int rc = resolve_dtt(dt_transform, p.dtt);
+    if (rc != SSD_OK) return rc;
+    p.batch = s.batch; p.H = s.nheads; p.P = s.headdim; p.N = s.dstate; p.G = s.ngroups;
+    p.dtype = s.dtype;
+    if (p.batch == 0) return SSD_OK;
+    if (!x || !dt || !A || !B || !C || !state || !y) return SSD_ERR_INVALID_ARG;
+    const size_t esz = p.dtype == SSD_F32 ? 4 : 2;
+    if (!aligned(x, esz) || !aligned(B, esz) || !aligned(C, esz) || !aligned(y, esz) ||
+        !aligned(dt, 4) || !aligned(A, 4) || !aligned(D, 4) || !aligned(state, 4))
+        return SSD_ERR_UNSUPPORTED;
+    p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D; p.state = state; p.y = y;
+    p.stream = (cudaStream_t)stream;
+    return step_launch(p) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
 SSD_API int ssd_check_device_status(const void *workspace, void *stream) {

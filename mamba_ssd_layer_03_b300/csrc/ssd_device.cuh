@@ -40,4 +40,20 @@ __device__ __forceinline__ bool status_bad(const int *status) {
     return *(volatile const int *)status != 0;
 }
 
+// The step-size transform of ssd_dt_transform (include/ssd.h): bias, then
+// softplus log(1 + e^z) (z itself above 20, where the two agree to fp32
+// precision), then the clamp.
+struct DtTransform {
+    const float *bias = nullptr;
+    int softplus = 0;
+    float lo = 0.f, hi = 0.f;
+    bool on = false;
+};
+
+__device__ __forceinline__ float dt_apply(float raw, float bias, int softplus, float lo, float hi) {
+    float z = raw + bias;
+    if (softplus) z = z > 20.f ? z : log1pf(expf(z));
+    return fminf(fmaxf(z, lo), hi);
+}
+
 }  // namespace ssd

@@ -74,6 +74,7 @@ struct FArgs {
     int *hflag;                // [grid] handoff published by ticket i
     float *hslot;              // [grid][2][P][N] handoff states
     const int *seqblk;         // [nseq + 1] prefix of blocks per sequence (varlen)
+    DtTransform dtt;           // step-size transform applied as dt is read
 };
 
 // One block of a CTA's walk as the compute warps need it, written by the TMA
@@ -96,6 +97,7 @@ struct BDesc {
     int h0, nh, s;       // first head, heads in the lane (1 or 2), sequence
     int flags;
     float A[2], D[2];    // per head of the lane (0 for a missing second head)
+    float bias[2];       // dt bias of the step-size transform (0 without one)
 };
 constexpr int kDescRing = 4;
 
@@ -425,6 +427,8 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     d.A[1] = ln.nh > 1 ? __ldg(a.A + ln.h0 + 1) : 0.f;
                     d.D[0] = a.D ? __ldg(a.D + ln.h0) : 0.f;
                     d.D[1] = (a.D && ln.nh > 1) ? __ldg(a.D + ln.h0 + 1) : 0.f;
+                    d.bias[0] = a.dtt.bias ? __ldg(a.dtt.bias + ln.h0) : 0.f;
+                    d.bias[1] = (a.dtt.bias && ln.nh > 1) ? __ldg(a.dtt.bias + ln.h0 + 1) : 0.f;
                     mbar_arrive(&sm->desc_full[k % kDescRing]);
                 }
                 if (k >= 2) fwait(&sm->x_empty[slot], ((k >> 1) + 1) & 1, a.status);
@@ -560,7 +564,9 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 // (a) dt and the within-block cumulative decay cs of head h
                 if (!have_next) prefetch_dt(dk, 0, slot);
                 asm volatile("cp.async.wait_all;" ::: "memory");
-                const float d = sm->dtn[slot][h][t];
+                float d = sm->dtn[slot][h][t];
+                if (a.dtt.on && hv && t < dk.rem)
+                    d = dt_apply(d, dk.bias[h], a.dtt.softplus, a.dtt.lo, a.dtt.hi);
                 have_next = (flags & kHasNext) != 0;
                 if (have_next) prefetch_dt(dk, kB, slot ^ 1);
                 float incl = d * dk.A[h];
@@ -1010,6 +1016,7 @@ cudaError_t fused_launch(const Problem &p) {
     a.nb_fixed = (int)((p.seqlen + kB - 1) / kB);
     a.grid = w.grid;
     a.dt = p.dt; a.A = p.A; a.D = p.D; a.init = p.init; a.cu = p.cu;
+    a.dtt = p.dtt;
     a.y = (bf16 *)p.y;
     a.final_states = p.final_states;
     a.status = p.status;

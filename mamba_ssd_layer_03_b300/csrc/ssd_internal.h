@@ -7,6 +7,7 @@
 #include <stddef.h>
 
 #include "../../include/ssd.h"
+#include "ssd_device.cuh"
 
 namespace ssd {
 
@@ -20,6 +21,7 @@ struct Problem {
     const float *dt = nullptr, *A = nullptr;
     const void *B = nullptr, *C = nullptr;
     const float *D = nullptr, *init = nullptr;
+    DtTransform dtt;      // applied by the fused kernel as it reads dt
     const int32_t *cu = nullptr;
     void *y = nullptr;
     float *final_states = nullptr;
@@ -46,6 +48,22 @@ cudaError_t tc_launch(const Problem &p);
 size_t fused_workspace_bytes(const Problem &p);
 int fused_supported(const Problem &p);
 cudaError_t fused_launch(const Problem &p);
+
+// ---- decode step (ssd_step.cu) ----
+struct StepProblem {
+    int64_t batch = 0;
+    int H = 0, P = 0, N = 0, G = 0, dtype = 0;
+    const void *x = nullptr, *B = nullptr, *C = nullptr;
+    const float *dt = nullptr, *A = nullptr, *D = nullptr;
+    DtTransform dtt;
+    float *state = nullptr;
+    void *y = nullptr;
+    cudaStream_t stream = nullptr;
+};
+cudaError_t step_launch(const StepProblem &p);
+
+// ---- step-size pre-pass (ssd_step.cu): dt' of every token into `out` ----
+cudaError_t launch_dt_transform(const Problem &p, float *out);
 
 // ---- shared helpers (ssd_api.cu) ----
 // Device check of cu_seqlens: cu[0]==0, cu[nseq]==seqlen, non-decreasing.

@@ -18,6 +18,15 @@ Two independent formulations, both in fp64:
   sum is formed directly as a sum over its own range, never as a difference
   of two cumulative sums.
 
+Two helpers around them, also fp64:
+
+* ``dt_transform`` -- the step size Delta = tau_Delta(parameter + s_Delta(x))
+  with tau_Delta = softplus (Mamba-1 walkthrough, section 三(二)): a bias per
+  head, softplus, then an optional clamp.
+* ``step`` -- one decode step, i.e. the recurrence over a single token with
+  the given state as the initial state (the recurrent mode used for
+  inference: Mamba-1 walkthrough, sections 二(一) and 四(五)).
+
 Readings taken where the pages are silent (one A scalar per head, Bbar = dt B,
 y from the updated state, an optional D skip term, contiguous head -> group
 mapping, exact state reset at packed-sequence boundaries) are shared by both
@@ -158,6 +167,30 @@ def recurrent_unit(x, dt, A, B, C, D, initial_states, cu_seqlens, s: int, h: int
     y, fin = recurrent(sl(x, h), dt[row:row + 1, t0:t1, h:h + 1], A[h:h + 1], sl(B, g), sl(C, g),
                        None if D is None else D[h:h + 1], S0, None, nthreads=1)
     return y[0, :, 0, :], fin[0, 0]
+
+
+def dt_transform(dt, bias=None, softplus: bool = False, dt_min: float = 0.0,
+                 dt_max: float = float("inf")) -> np.ndarray:
+    """fp64 step sizes dt' = clamp(softplus(dt + bias[h])) for dt (..., H).
+    softplus(z) = log(1 + e^z), evaluated as logaddexp(0, z) so that it
+    neither overflows for large z nor loses e^z for very negative z."""
+    z = _f64(dt)
+    if bias is not None:
+        z = z + _f64(bias)
+    if softplus:
+        z = np.logaddexp(0.0, z)
+    return np.minimum(np.maximum(z, dt_min), dt_max)
+
+
+def step(x, dt, A, B, C, D, state):
+    """fp64 decode step of sequences holding one token each: x (b, H, P),
+    dt (b, H), B/C (b, G, N), state (b, H, P, N).  Returns (y (b, H, P),
+    new state (b, H, P, N)): the recurrence over that single token starting
+    from `state`."""
+    x, dt, B, C = (_f64(t) for t in (x, dt, B, C))
+    y, fin = recurrent(x[:, None], dt[:, None], A, B[:, None], C[:, None], D,
+                       initial_states=state)
+    return y[:, 0], fin
 
 
 def quadratic(x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None):

@@ -79,7 +79,9 @@ def make_inputs(w: Workload, seed: int = 0, *, batch: Optional[int] = None,
     keep the distributions and change only the shape; tests use them for
     ragged and degenerate cases.
     Returns a dict with x, dt, A, B, C, D, initial_states (or None),
-    cu_seqlens (int32 or None) and the shape scalars.
+    cu_seqlens (int32 or None) and the shape scalars, plus the parts dt is
+    made of (dt_raw = the noise n, dt_bias = bias_h), for the scan's optional
+    step-size transform.
     """
     b = w.batch if batch is None else batch
     L = w.seqlen if seqlen is None else seqlen
@@ -136,4 +138,12 @@ def make_inputs(w: Workload, seed: int = 0, *, batch: Optional[int] = None,
         C=Cm.to(dt_store).contiguous(), D=D.float().contiguous(),
         initial_states=None if init is None else init.float().contiguous(),
         cu_seqlens=cu, batch=b, seqlen=L, nheads=H, headdim=P, dstate=N,
-        ngroups=G, chunk=w.chunk, nseq=nseq, dtype=w.dtype)
+        ngroups=G, chunk=w.chunk, nseq=nseq, dtype=w.dtype,
+        dt_raw=dt_noise.float().contiguous(), dt_bias=bias.float().contiguous())
+
+
+def make_dt_parts(w: Workload, seed: int = 0, **shape):
+    """(dt_raw, dt_bias, dt) of the input set make_inputs(w, seed, **shape)
+    draws: dt = softplus(dt_raw + dt_bias[h])."""
+    inp = make_inputs(w, seed, **shape)
+    return inp["dt_raw"], inp["dt_bias"], inp["dt"]

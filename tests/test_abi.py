@@ -111,3 +111,87 @@ def test_scan_rejects_on_host_before_device_work():
 
 def test_check_status_rejects_null():
     assert ssd.load_library().ssd_check_device_status(None, None) == 1
+
+
+# ---------------------------------------------------------------- step-size transform
+
+def test_scan_ex_workspace_with_transform():
+    tf = ssd.SsdDtTransform(None, 1, 0.0, float("inf"))
+    # the fused kernel applies the transform inline: no extra workspace (its
+    # workspace depends on the device's SM count, so this part needs a GPU)
+    base = _shape(algo="tc")
+    try:
+        plain = ssd.workspace_size(base)
+    except ssd.SsdError:
+        plain = None
+    if plain is not None:
+        assert ssd.workspace_size(base, tf) == plain
+    # the other paths transform dt into the end of the workspace first
+    for algo in ("simt", "tc2"):
+        sh = _shape(algo=algo)
+        try:
+            plain = ssd.workspace_size(sh)
+        except ssd.SsdError:
+            continue   # sized from the device's properties: needs a GPU
+        assert ssd.workspace_size(sh, tf) - plain >= 4 * 8192 * 80 * 4, algo
+
+
+def test_scan_ex_rejects_bad_transform():
+    lib = ssd.load_library()
+    n = ctypes.c_size_t(0)
+    for lo, hi in ((1.0, 0.5), (float("nan"), 1.0)):
+        tf = ssd.SsdDtTransform(None, 1, lo, hi)
+        assert lib.ssd_scan_ex_workspace_size(ctypes.byref(_shape()), ctypes.byref(tf),
+                                              ctypes.byref(n)) == 1
+
+
+# ---------------------------------------------------------------- decode step
+
+def _step_shape(**kw):
+    d = dict(batch=4, nheads=80, headdim=64, dstate=128, ngroups=1, dtype=ssd.SSD_BF16,
+             reserved=0)
+    d.update(kw)
+    return ssd.SsdStepShape(d["batch"], d["nheads"], d["headdim"], d["dstate"], d["ngroups"],
+                            d["dtype"], d["reserved"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(nheads=0), 1),
+    (dict(ngroups=3), 1),
+    (dict(reserved=1), 1),
+    (dict(batch=-1), 1),
+    (dict(dtype=7), 2),
+    (dict(headdim=2048), 2),
+    (dict(dstate=2048), 2),
+])
+def test_step_rejects_bad_shapes_on_host(kw, code):
+    lib = ssd.load_library()
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: validation fails first
+    sh = _step_shape(**kw)
+    assert lib.ssd_step(ctypes.byref(sh), fake, fake, None, fake, fake, fake, None, fake, fake,
+                        None) == code
+
+
+def test_step_rejects_null_and_misaligned_pointers():
+    lib = ssd.load_library()
+    fake = ctypes.c_void_p(1 << 20)
+    sh = _step_shape()
+    assert lib.ssd_step(None, fake, fake, None, fake, fake, fake, None, fake, fake, None) == 1
+    assert lib.ssd_step(ctypes.byref(sh), None, fake, None, fake, fake, fake, None, fake, fake,
+                        None) == 1
+    assert lib.ssd_step(ctypes.byref(sh), fake, fake, None, fake, fake, fake, None, None, fake,
+                        None) == 1
+    odd = ctypes.c_void_p((1 << 20) + 1)
+    assert lib.ssd_step(ctypes.byref(sh), odd, fake, None, fake, fake, fake, None, fake, fake,
+                        None) == 2
+    tf = ssd.SsdDtTransform(None, 1, 2.0, 1.0)
+    assert lib.ssd_step(ctypes.byref(sh), fake, fake, ctypes.byref(tf), fake, fake, fake, None,
+                        fake, fake, None) == 1
+
+
+def test_step_zero_batch_is_a_no_op():
+    # nothing is enqueued, so null data pointers are fine
+    lib = ssd.load_library()
+    sh = _step_shape(batch=0)
+    assert lib.ssd_step(ctypes.byref(sh), None, None, None, None, None, None, None, None, None,
+                        None) == 0

@@ -239,3 +239,76 @@ def test_planted_mistakes_are_caught(mutation):
 
 def test_unmutated_passes_the_same_pins():
     assert _pins_pass(None)
+
+
+# ---------------------------------------------------------------- step sizes
+# The step-size transform Delta = softplus(parameter + s_Delta(x)) (Mamba-1
+# walkthrough, section 三(二)), clamp last.  Pinned by values and identities
+# of softplus, not by retyping it.
+
+def test_dt_transform_softplus_values():
+    z = np.array([[0.0, math.log(math.e - 1.0), 50.0, -50.0]])
+    got = oracle.dt_transform(z, softplus=True)
+    assert got[0, 0] == pytest.approx(math.log(2.0), rel=1e-15)     # log(1 + 1)
+    assert got[0, 1] == pytest.approx(1.0, rel=1e-15)               # log(1 + (e - 1)) = 1
+    assert got[0, 2] == pytest.approx(50.0, rel=1e-15)              # log(1 + e^50) = 50 + log1p(e^-50)
+    assert got[0, 3] == pytest.approx(math.exp(-50.0), rel=1e-12)   # log(1 + e^-50) ~ e^-50
+
+
+def test_dt_transform_softplus_identity_and_bias():
+    g = torch.Generator().manual_seed(5)
+    z = torch.randn(3, 7, 4, generator=g, dtype=torch.float64).numpy() * 6
+    sp = oracle.dt_transform(z, softplus=True)
+    sm = oracle.dt_transform(-z, softplus=True)
+    # softplus(z) - softplus(-z) = z, and softplus(z) > max(z, 0)
+    np.testing.assert_allclose(sp - sm, z, rtol=0, atol=1e-12)
+    assert np.all(sp > np.maximum(z, 0.0))
+    bias = np.array([0.5, -1.0, 2.0, 0.0])
+    np.testing.assert_array_equal(oracle.dt_transform(z, bias=bias, softplus=True),
+                                  oracle.dt_transform(z + bias, softplus=True))
+    # no softplus: the bias alone, then the default clamp at 0 (step sizes are
+    # never negative); with no lower bound it is the plain sum
+    np.testing.assert_array_equal(oracle.dt_transform(z, bias=bias), np.maximum(z + bias, 0.0))
+    np.testing.assert_array_equal(oracle.dt_transform(z, bias=bias, dt_min=-np.inf), z + bias)
+
+
+def test_dt_transform_clamp():
+    z = np.array([[-3.0, 0.2, 0.5, 9.0]])
+    np.testing.assert_array_equal(oracle.dt_transform(z, dt_min=0.1, dt_max=1.0),
+                                  [[0.1, 0.2, 0.5, 1.0]])
+    got = oracle.dt_transform(z, softplus=True, dt_min=0.5, dt_max=2.0)
+    assert got[0, 0] == 0.5 and got[0, 3] == 2.0
+
+
+def test_dt_transform_reproduces_the_generators_step_sizes():
+    # the synthetic inputs draw dt = softplus(noise + inv_softplus(dt0)) with
+    # torch's softplus; the oracle's transform of (noise, bias) must agree
+    w = ssd_synth.WORKLOADS[1]
+    raw, bias, dt = ssd_synth.make_dt_parts(w, seed=3, batch=2, seqlen=64, nheads=6)
+    got = oracle.dt_transform(raw.double(), bias=bias.double(), softplus=True)
+    np.testing.assert_allclose(got, dt.double().numpy(), rtol=1e-6, atol=0)
+
+
+# ---------------------------------------------------------------- decode step
+
+def test_step_equals_recurrence_token_by_token():
+    c = _rand_case(21, b=2, L=9, H=4, P=3, N=5, G=2)
+    x, dt, A, B, C, D, S0 = (c[k] for k in ("x", "dt", "A", "B", "C", "D", "initial_states"))
+    y_ref, fin_ref = oracle.recurrent(**c)
+    S = S0.numpy().copy()
+    for t in range(9):
+        y, S = oracle.step(x[:, t], dt[:, t], A, B[:, t], C[:, t], D, S)
+        np.testing.assert_allclose(y, y_ref[:, t], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(S, fin_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_step_closed_form():
+    # one token: S' = e^{dt A} S + dt x B^T, y = S' C + D x, written out by hand
+    c = _rand_case(22, b=1, L=1, H=2, P=2, N=3, G=1)
+    x, dt, A, B, C, D, S0 = (c[k] for k in ("x", "dt", "A", "B", "C", "D", "initial_states"))
+    y, S = oracle.step(x[:, 0], dt[:, 0], A, B[:, 0], C[:, 0], D, S0)
+    for h in range(2):
+        d = float(dt[0, 0, h])
+        Sp = math.exp(d * float(A[h])) * S0[0, h].numpy() + d * np.outer(x[0, 0, h].numpy(), B[0, 0, 0].numpy())
+        np.testing.assert_allclose(S[0, h], Sp, rtol=1e-13)
+        np.testing.assert_allclose(y[0, h], Sp @ C[0, 0, 0].numpy() + float(D[h]) * x[0, 0, h].numpy(), rtol=1e-13)
