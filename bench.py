@@ -11,6 +11,10 @@ the workload (independent problems: weak scaling, no collective on the data
 path); rank 0 prints one JSON line.
 ``--impl reference`` times the CPU oracle on the host cores instead (a bounded
 sample of the same workload per step).
+
+``--op step`` measures the decode step instead (ssd_step: one token for each
+of 64 sequences of the 2.7B-shaped layer, the fp32 state updated in place),
+with its own JSON line.
 """
 from __future__ import annotations
 
@@ -246,6 +250,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seqlen", type=int, default=None,
                     help="override the workload's tokens per sequence (profiling captures)")
+    ap.add_argument("--op", default="scan", choices=["scan", "step"])
+    ap.add_argument("--step-batch", type=int, default=64,
+                    help="sequences per decode step (--op step)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -255,6 +262,8 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args, w, rank, world)
+    if args.op == "step":
+        return run_step_bench(args, w, rank, world, local)
 
     dist = None
     if world > 1:
@@ -402,6 +411,155 @@ def main():
         if args.seqlen is not None:
             out["config"]["seqlen_override"] = args.seqlen
         out["gpu_launches"] = launches_per_step(algo, inp) * args.steps
+        print(json.dumps(out))
+    if dist:
+        dist.destroy_process_group()
+
+
+def step_inputs(w, batch, seed):
+    """One decode step's inputs for the shape of workload w: the token of each
+    sequence drawn like the workload's tokens (seeded), the states ~ N(0, 0.1)."""
+    inp = ssd_synth.make_inputs(w, seed=seed, batch=batch, seqlen=1)
+    g = torch.Generator().manual_seed(seed + 1000)
+    state = torch.randn(batch, inp["nheads"], inp["headdim"], inp["dstate"], generator=g) * 0.1
+    return dict(x=inp["x"][:, 0].contiguous(), dt=inp["dt"][:, 0].contiguous(), A=inp["A"],
+                B=inp["B"][:, 0].contiguous(), C=inp["C"][:, 0].contiguous(), D=inp["D"],
+                state=state.contiguous(), dtype=inp["dtype"])
+
+
+def step_cost(inp):
+    """Algorithmic bytes of one decode step: the state read and written once,
+    x, y, B, C, dt, A, D once."""
+    nb = lambda t: t.numel() * t.element_size()
+    return (2 * nb(inp["state"]) + 2 * nb(inp["x"]) + nb(inp["B"]) + nb(inp["C"]) + nb(inp["dt"])
+            + nb(inp["A"]) + nb(inp["D"]))
+
+
+def run_step_bench(args, w, rank, world, local):
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import mamba_ssd_layer_03_b300 as ssd
+
+    inp = step_inputs(w, args.step_batch, seed=rank)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y = torch.empty_like(d["x"])
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ssd.ssd_step(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["state"], out=y)
+
+    nbytes = step_cost(inp)
+    peaks = load_peaks()
+    steps = max(args.steps, 1)
+    # A decode loop replays its steps as a CUDA graph: one launch each, no
+    # host time between them.  The K timed steps are one captured graph.
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(steps):
+            step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    with sampler:
+        time.sleep(0.3)
+        for _ in range(max(args.warmup, 3)):
+            graph.replay()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_host0 = time.perf_counter()
+        ev0.record(stream)
+        graph.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        t_host1 = time.perf_counter()
+        if dist:
+            dist.barrier()
+        time.sleep(0.15)
+    total_ms = ev0.elapsed_time(ev1)
+    tokens = inp["x"].shape[0]
+    total_ms, value = aggregate_over_ranks(total_ms, tokens, steps, dist, dev)
+    ms = total_ms / steps
+    achieved = nbytes / (ms / 1e3) / 1e9
+
+    e2e = None
+    if rank == 0 or world > 1:
+        # a decode loop keeps the state on the device; each step's token
+        # (x, dt, B, C) comes from the host and y goes back
+        in_keys = ("x", "dt", "B", "C")
+        host = {k: inp[k].pin_memory() for k in in_keys}
+        dbuf = {k: torch.empty_like(d[k]) for k in in_keys}
+        y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        h2d = sum(host[k].numel() * host[k].element_size() for k in in_keys)
+        d2h = y_host.numel() * y_host.element_size()
+
+        def e2e_step():
+            for k in in_keys:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            ssd.ssd_step(dbuf["x"], dbuf["dt"], d["A"], dbuf["B"], dbuf["C"], d["D"], d["state"],
+                         out=y)
+            y_host.copy_(y, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        k_e2e = max(3, min(steps, 50))
+        for _ in range(k_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / k_e2e
+        e2e = {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        reps = 0
+        t0 = time.perf_counter()
+        while True:
+            oracle.step(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["state"])
+            reps += 1
+            if time.perf_counter() - t0 > min(args.cpu_budget, 10.0):
+                break
+        secs = time.perf_counter() - t0
+        cpu = {"value": reps * tokens / secs, "unit": "tokens/s", "cores": oracle.max_threads(),
+               "kind": "oracle", "sample": f"{reps} full decode steps of the same batch, fp64, "
+                                           f"{secs:.1f} s"}
+
+    if rank == 0:
+        b, H, P = inp["x"].shape
+        N = inp["state"].shape[-1]
+        wname = f"decode_h{H}_p{P}_n{N}_b{b}"
+        out = {
+            "metric": "SSD decode step tokens/s (one token per sequence, state in place) on 1 B300",
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": inp["dtype"],
+            "data": "synthetic (seeded, the workload's distributions)",
+            "config": {"workload": wname, "batch": b, "nheads": H, "headdim": P,
+                       "dstate": N, "ngroups": inp["B"].shape[1], "launch": "cuda graph of the timed steps",
+                       "parallelism": f"replicas x{world} (independent problems)",
+                       "l2": f"state larger than L2: {nbytes / 1e6:.0f} MB streamed per step vs "
+                             f"{L2_BYTES / 2**20:.0f} MiB L2, no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": profiled_traffic("ssd_step.cu", wname),
+                         "peak_source": peaks["source"],
+                         "kernel": "k_ssd_step (timed as the whole ssd_step call)",
+                         "algorithmic_bytes": nbytes, "kernel_ms": ms},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": steps,
+            "clocks": sampler.summary(t_host0, t_host1),
+        }
         print(json.dumps(out))
     if dist:
         dist.destroy_process_group()

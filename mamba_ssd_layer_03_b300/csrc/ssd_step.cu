@@ -39,8 +39,10 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // One CTA per (sequence b, head h).  B and C of the token go to shared memory
 // as fp32.  Warp w updates state rows p = 4w .. 4w + 3, then 4w + 32 ... (four
-// rows' loads in flight); lane l holds columns n = 4 (l + 32 i) .. + 3 when
-// N % 4 == 0 (16-byte accesses, coalesced along the row), else n = l + 32 i.
+// rows' loads in flight; eight raise the registers to 128 and the lost
+// occupancy costs more than the deeper queue gains); lane l holds columns
+// n = 4 (l + 32 i) .. + 3 when N % 4 == 0 (16-byte accesses, coalesced along
+// the row), else n = l + 32 i.
 // The row's y is the warp's sum of S[p, n] C[n], plus D_h x[p].
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kStepThreads) k_ssd_step(StepArgs a) {
