@@ -357,6 +357,9 @@ __device__ __noinline__ void mask_chunk_exact(uint32_t taddr, float cs0, float c
 // ----------------------------------------------------------------------------
 // the kernel
 
+// kDtTransform: the step-size transform is compiled in only where a call asks
+// for it, so the plain scan carries no trace of it.
+template <bool kDtTransform>
 __global__ void __launch_bounds__(kThreads, 1)
 k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmY,
@@ -565,7 +568,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 if (!have_next) prefetch_dt(dk, 0, slot);
                 asm volatile("cp.async.wait_all;" ::: "memory");
                 float d = sm->dtn[slot][h][t];
-                if (a.dtt.on && hv && t < dk.rem)
+                if (kDtTransform && hv && t < dk.rem)
                     d = dt_apply(d, dk.bias[h], a.dtt.softplus, a.dtt.lo, a.dtt.hi);
                 have_next = (flags & kHasNext) != 0;
                 if (have_next) prefetch_dt(dk, kB, slot ^ 1);
@@ -1042,10 +1045,10 @@ cudaError_t fused_launch(const Problem &p) {
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    e = cudaFuncSetAttribute(k_ssd_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes);
+    auto kern = a.dtt.on ? k_ssd_fused<true> : k_ssd_fused<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    k_ssd_fused<<<w.grid, kThreads, kSmemBytes, p.stream>>>(tmX, tmB, tmC, tmY, a);
+    kern<<<w.grid, kThreads, kSmemBytes, p.stream>>>(tmX, tmB, tmC, tmY, a);
     return cudaGetLastError();
 }
 
