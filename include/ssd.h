@@ -84,10 +84,10 @@ typedef enum ssd_algo {
     SSD_ALGO_AUTO = 0,     /* tensor-core path when the shape allows, else SIMT */
     SSD_ALGO_SIMT = 1,     /* CUDA-core kernels, any supported shape/dtype */
     SSD_ALGO_TC = 2,       /* tcgen05/TMEM/TMA path (bf16 only): the fused
-                              single-pass kernel for headdim 64 / dstate 128
-                              (any chunk size, packed sequences included),
-                              else the two-pass kernels; UNSUPPORTED if the
-                              shape fits neither */
+                              single-pass kernel for headdim 64 and dstate
+                              128 or 256 (any chunk size, packed sequences
+                              included), else the two-pass kernels;
+                              UNSUPPORTED if the shape fits neither */
     SSD_ALGO_TC_TWOPASS = 3 /* the two-pass tensor-core kernels (chunk-state
                               scan, then chunk output): bf16, headdim 64,
                               dstate 128 or 256, chunk 128 or 256, no packed

@@ -58,12 +58,26 @@ typedef __nv_bfloat16 bf16;
 constexpr int kB = 128;                    // tokens per block
 constexpr int kThreads = 320;              // 8 compute warps + TMA warp + MMA warp
 constexpr uint32_t kT16 = 16384;           // one 128-row x 128-byte swizzled tile
-constexpr int kP = 64, kN = 128;           // headdim and dstate of this path
-constexpr int kStateFloats = 2 * kP * kN;  // state of one lane (two heads)
+constexpr int kP = 64;                     // headdim of this path
+constexpr int kStateFloats = 2 * kP * 128; // state of one lane: 2 heads x 128 or 1 head x 256
+
+// Lane geometry.  Narrow: dstate 128, two heads of a group per lane.  Wide:
+// dstate 256, one head per lane; its state's two 128-row halves go to the two
+// warpgroups, which for the narrow kernel hold the two heads.
+template <bool kWide>
+struct Geo {
+    static constexpr int N = kWide ? 256 : 128;     // dstate
+    static constexpr int HL = kWide ? 1 : 2;        // heads per lane
+    static constexpr int NA = N / 64;               // 64-wide n atoms of a C or B tile
+    static constexpr uint32_t ACC = kP * HL;        // TMEM columns of one accumulator
+    // shared-memory tiles of 16 KB: C, B, X (2 slots), Xw, H_op
+    static constexpr int TILES = 2 * NA + 2 * HL + HL + 2;
+};
 
 struct FArgs {
     int64_t L;                 // tokens per batch row
-    int H, G, hpg, npg, ptot;  // heads, groups, heads per group, pairs per group, pairs
+    int H, G, hpg, npg, ptot;  // heads, groups, heads per group, lanes per group, lanes per sequence
+    int hpl;                   // heads per lane (2 narrow, 1 wide)
     int nseq, varlen, nb_fixed, grid;
     const float *dt, *A, *D, *init;
     const int32_t *cu;
@@ -118,8 +132,8 @@ struct Smem {
     int ticket;
 };
 
-constexpr size_t kTileBytes = 12 * (size_t)kT16;  // C, B, X[2], Xw, H_op in 16 KB atoms
-constexpr size_t kSmemBytes = 1024 + kTileBytes + sizeof(Smem);
+template <bool kWide>
+constexpr size_t smem_bytes() { return 1024 + (size_t)Geo<kWide>::TILES * kT16 + sizeof(Smem); }
 
 // ----------------------------------------------------------------------------
 // lanes and blocks
@@ -142,8 +156,8 @@ __device__ __forceinline__ Lane lane_info(const FArgs &a, int64_t l) {
     const int pair = (int)(l % a.ptot);
     n.g = pair / a.npg;
     const int k = pair % a.npg;
-    n.h0 = n.g * a.hpg + 2 * k;
-    n.nh = min(2, a.hpg - 2 * k);
+    n.h0 = n.g * a.hpg + a.hpl * k;
+    n.nh = min(a.hpl, a.hpg - a.hpl * k);
     if (a.varlen) {
         const int c0 = __ldg(a.cu + n.s), c1 = __ldg(a.cu + n.s + 1);
         n.row = 0;
@@ -359,18 +373,20 @@ __device__ __noinline__ void mask_chunk_exact(uint32_t taddr, float cs0, float c
 
 // kDtTransform: the step-size transform is compiled in only where a call asks
 // for it, so the plain scan carries no trace of it.
-template <bool kDtTransform>
+template <bool kDtTransform, bool kWide>
 __global__ void __launch_bounds__(kThreads, 1)
 k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmY,
             FArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *sC = base;                  // [n atom][128 rows][64]        32 KB
-    uint8_t *sB = sC + 2 * kT16;         // [n atom][128 rows][64]        32 KB
-    uint8_t *sX = sB + 2 * kT16;         // [slot][head][128 rows][64]    64 KB
-    uint8_t *sXw = sX + 4 * kT16;        // [head][128 rows][64]          32 KB
-    uint8_t *sH = sXw + 2 * kT16;        // [head][128 n rows][64 p]      32 KB
+    using Gm = Geo<kWide>;
+    constexpr int HL = Gm::HL, NA = Gm::NA, NS = Gm::N;
+    uint8_t *sC = base;                   // [n atom][128 rows][64]        NA x 16 KB
+    uint8_t *sB = sC + NA * kT16;         // [n atom][128 rows][64]        NA x 16 KB
+    uint8_t *sX = sB + NA * kT16;         // [slot][head][128 rows][64]    2 HL x 16 KB
+    uint8_t *sXw = sX + 2 * HL * kT16;    // [head][128 rows][64]          HL x 16 KB
+    uint8_t *sH = sXw + HL * kT16;        // narrow [head][128 n][64 p], wide [256 n][64 p]: 32 KB
     Smem *sm = (Smem *)(sH + 2 * kT16);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -435,18 +451,18 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     mbar_arrive(&sm->desc_full[k % kDescRing]);
                 }
                 if (k >= 2) fwait(&sm->x_empty[slot], ((k >> 1) + 1) & 1, a.status);
-                for (int s = 0; s < 2; ++s)
-                    tma_load_4d(sX + (size_t)(slot * 2 + s) * kT16, &tmX, &sm->x_full[slot], 0,
+                for (int s = 0; s < HL; ++s)
+                    tma_load_4d(sX + (size_t)(slot * HL + s) * kT16, &tmX, &sm->x_full[slot], 0,
                                 w.ln.h0 + s, tok, w.ln.row);
-                mbar_arrive_expect_tx(&sm->x_full[slot], 2 * kT16);
+                mbar_arrive_expect_tx(&sm->x_full[slot], HL * kT16);
                 if (k >= 1) fwait(&sm->c_empty, (k - 1) & 1, a.status);
-                for (int nb = 0; nb < 2; ++nb)
+                for (int nb = 0; nb < NA; ++nb)
                     tma_load_4d(sC + nb * kT16, &tmC, &sm->c_full, nb * 64, w.ln.g, tok, w.ln.row);
-                mbar_arrive_expect_tx(&sm->c_full, 2 * kT16);
+                mbar_arrive_expect_tx(&sm->c_full, NA * kT16);
                 if (k >= 1) fwait(&sm->b_empty, (k - 1) & 1, a.status);
-                for (int nb = 0; nb < 2; ++nb)
+                for (int nb = 0; nb < NA; ++nb)
                     tma_load_4d(sB + nb * kT16, &tmB, &sm->b_full, nb * 64, w.ln.g, tok, w.ln.row);
-                mbar_arrive_expect_tx(&sm->b_full, 2 * kT16);
+                mbar_arrive_expect_tx(&sm->b_full, NA * kT16);
             }
             // let every copy this thread started land before the CTA exits
             if (k >= 1) {
@@ -459,32 +475,34 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA
         if (lane == 0 && run) {
+            // Ys and S have N = 64 per head: 128 with two heads, 64 with one
             const uint32_t id_cb = idesc_bf16_f32(128, 128, 0, 0);
-            const uint32_t id_ys = idesc_bf16_f32(128, 128, 0, 1);
-            const uint32_t id_s = idesc_bf16_f32(128, 128, 1, 1);
+            const uint32_t id_ys = idesc_bf16_f32(128, 64 * HL, 0, 1);
+            const uint32_t id_s = idesc_bf16_f32(128, 64 * HL, 1, 1);
             const uint32_t id_mx = idesc_bf16_f32(128, 64, 0, 1);
             const uint32_t sc = smem_u32(sC), sbb = smem_u32(sB), sxw = smem_u32(sXw),
                            sh = smem_u32(sH), sx = smem_u32(sX);
             const uint32_t nblk = (uint32_t)cta_blocks(a, ticket);
             for (uint32_t k = 0; k < nblk; ++k) {
                 const int slot = k & 1;
-                const uint32_t R_acc = tbase + 256 + 128 * slot;
+                const uint32_t R_acc = tbase + 256 + Gm::ACC * slot;
                 fwait(&sm->c_full, k & 1, a.status);
                 fwait(&sm->b_full, k & 1, a.status);
                 tc_fence_after();
                 // CB = C B^T (over the previous block's M, read by its last product)
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < 4 * NA; ++kk) {
                     const uint32_t off = (uint32_t)(kk >> 2) * kT16 + (uint32_t)(kk & 3) * 32;
                     mma_ss(R_cb, smem_desc(sc + off, 16, 1024, kSwizzle128B),
                            smem_desc(sbb + off, 16, 1024, kSwizzle128B), id_cb, kk > 0);
                 }
-                // Ys = C H^T (both heads stacked along N)
+                // Ys = C H^T (narrow: both heads stacked along N; wide: K = 256
+                // over H_op's 256 n rows)
                 fwait(&sm->hop_ready, k & 1, a.status);
                 if (k >= 2) fwait(&sm->acc_free[slot], ((k >> 1) + 1) & 1, a.status);
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < 4 * NA; ++kk) {
                     const uint32_t off = (uint32_t)(kk >> 2) * kT16 + (uint32_t)(kk & 3) * 32;
                     mma_ss(R_acc, smem_desc(sc + off, 16, 1024, kSwizzle128B),
                            smem_desc(sh + kk * 2048, kT16, 1024, kSwizzle128B), id_ys, kk > 0);
@@ -495,22 +513,26 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 fwait(&sm->xw_ready, k & 1, a.status);
                 fwait(&sm->x_full[slot], (k >> 1) & 1, a.status);
                 tc_fence_after();
-                // H <- (decay H, already in TMEM) + B^T Xw
+                // H <- (decay H, already in TMEM) + B^T Xw; wide: one product
+                // per 128-row half of n (B tile atoms 2q, 2q + 1)
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(R_H, smem_desc(sbb + kk * 2048, kT16, 1024, kSwizzle128B),
-                           smem_desc(sxw + kk * 2048, kT16, 1024, kSwizzle128B), id_s, 1);
+                for (int q = 0; q < (kWide ? 2 : 1); ++q)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(R_H + 64 * q,
+                               smem_desc(sbb + 2 * q * kT16 + kk * 2048, kT16, 1024, kSwizzle128B),
+                               smem_desc(sxw + kk * 2048, kT16, 1024, kSwizzle128B), id_s, 1);
                 mma_commit(&sm->s_done);
                 mma_commit(&sm->b_empty);
                 // acc_h += M_h x_h (M from TMEM)
                 fwait(&sm->m_ready, k & 1, a.status);
                 tc_fence_after();
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
+                for (int hh = 0; hh < HL; ++hh)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ts(R_acc + hh * 64, R_cb + m_col(kk, hh),
-                               smem_desc(sx + (uint32_t)(slot * 2 + hh) * kT16 + kk * 2048, kT16,
+                               smem_desc(sx + (uint32_t)(slot * HL + hh) * kT16 + kk * 2048, kT16,
                                          1024, kSwizzle128B),
                                id_mx, 1);
                 mma_commit(&sm->mx_done[slot]);
@@ -527,7 +549,11 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         // the state, the scan and the outputs the warpgroup works on head h of
         // the lane; for the masked block on C B^T columns [64 h, 64 h + 64)
         // for both heads.
+        // Wide lanes (one head, dstate 256): both warpgroups scan the lane's
+        // head; warpgroup h holds state rows n in [128 h, 128 h + 128), Xw and
+        // y chunks [4 h, 4 h + 4) of each row, and acc columns [32 h, 32 h + 32).
         const int h = warp >> 2;
+        const int hs = kWide ? 0 : h;     // head of the lane this warpgroup scans
         const int t = tid & 127;
         const int wq = warp & 3;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -539,8 +565,8 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         // or the lane's heads
         auto prefetch_dt = [&](const BDesc &dk, int off, int par) {
             float *dst = &sm->dtn[par][h][t];
-            if (h < dk.nh && off + t < dk.rem) {
-                const float *src = a.dt + ((int64_t)dk.row * a.L + dk.tok + off + t) * a.H + dk.h0 + h;
+            if (hs < dk.nh && off + t < dk.rem) {
+                const float *src = a.dt + ((int64_t)dk.row * a.L + dk.tok + off + t) * a.H + dk.h0 + hs;
                 asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)),
                              "l"(src) : "memory");
             } else {
@@ -558,10 +584,10 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 fwait(&sm->desc_full[k % kDescRing], (k / kDescRing) & 1, a.status);
                 const BDesc &dk = sm->desc[k % kDescRing];
                 const int flags = dk.flags;
-                const bool hv = h < dk.nh;
-                const int head = dk.h0 + (hv ? h : 0);
+                const bool hv = hs < dk.nh;
+                const int head = dk.h0 + (hv ? hs : 0);
                 const int slot = k & 1;
-                const uint32_t R_acc = tbase + 256 + 128 * slot;
+                const uint32_t R_acc = tbase + 256 + Gm::ACC * slot;
                 const bool seg_start = (flags & kSegStart) != 0;
 
                 // (a) dt and the within-block cumulative decay cs of head h
@@ -569,10 +595,10 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 asm volatile("cp.async.wait_all;" ::: "memory");
                 float d = sm->dtn[slot][h][t];
                 if (kDtTransform && hv && t < dk.rem)
-                    d = dt_apply(d, dk.bias[h], a.dtt.softplus, a.dtt.lo, a.dtt.hi);
+                    d = dt_apply(d, dk.bias[hs], a.dtt.softplus, a.dtt.lo, a.dtt.hi);
                 have_next = (flags & kHasNext) != 0;
                 if (have_next) prefetch_dt(dk, kB, slot ^ 1);
-                float incl = d * dk.A[h];
+                float incl = d * dk.A[hs];
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
                     const float v = __shfl_up_sync(0xffffffffu, incl, off);
@@ -609,12 +635,13 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                             }
                             __nanosleep(64);
                         }
-                        src = a.hslot + (size_t)(ticket - 1) * kStateFloats + h * kP * kN;
+                        src = a.hslot + (size_t)(ticket - 1) * kStateFloats + hs * kP * NS;
                         from_slot = true;
                     } else if (a.init && hv) {
-                        src = a.init + ((int64_t)dk.s * a.H + head) * kP * kN;
+                        src = a.init + ((int64_t)dk.s * a.H + head) * kP * NS;
                     }
                     if (!hv) src = nullptr;
+                    const int n_row = kWide ? 128 * h + t : t;   // this thread's state row
 #pragma unroll 1
                     for (int c4 = 0; c4 < kP / 4; ++c4) {
                         uint32_t r[4];
@@ -622,7 +649,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                         for (int q = 0; q < 4; ++q) {
                             float e = 0.f;
                             if (src) {
-                                const float *sp = src + (c4 * 4 + q) * kN + t;
+                                const float *sp = src + (c4 * 4 + q) * NS + n_row;
                                 e = from_slot ? __ldcg(sp) : __ldg(sp);
                             }
                             r[q] = __float_as_uint(e);
@@ -665,12 +692,14 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     tma_store_wait_read0();
                     pend_store = false;
                 }
-                named_bar(bar_wg, 128);   // the y store has read this half of Xw
+                // the y store has read this half of Xw (wide: the one tile
+                // both warpgroups write, stored by thread 0)
+                if (kWide) named_bar(3, 256); else named_bar(bar_wg, 128);
                 {
-                    const uint4 *src = (const uint4 *)(sX + (size_t)(slot * 2 + h) * kT16 + t * 128);
-                    uint4 *dst = (uint4 *)(sXw + h * kT16 + t * 128);
+                    const uint4 *src = (const uint4 *)(sX + (size_t)(slot * HL + hs) * kT16 + t * 128);
+                    uint4 *dst = (uint4 *)(sXw + hs * kT16 + t * 128);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = kWide ? 4 * h : 0; c < (kWide ? 4 * h + 4 : 8); ++c) {
                         const int pc = c ^ (t & 7);
                         const uint4 u = src[pc];
                         uint32_t ww[4] = {u.x, u.y, u.z, u.w};
@@ -736,11 +765,15 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                                     const float2 f0 = *(const float2 *)(vf0 + j0);
                                     const float2 f1 = *(const float2 *)(vf1 + j0);
                                     float a0 = c0 * u0 * f0.x, a1 = c1 * u0 * f0.y;
-                                    float b0 = c0 * u1 * f1.x, b1 = c1 * u1 * f1.y;
-                                    if (j0 == lim && own) { a0 += dd0; b0 += dd1; }
-                                    if (j1 == lim && own) { a1 += dd0; b1 += dd1; }
+                                    if (j0 == lim && own) a0 += dd0;
+                                    if (j1 == lim && own) a1 += dd0;
                                     pk0[q] = pack_bf16x2(a0, a1);
-                                    pk1[q] = pack_bf16x2(b0, b1);
+                                    if (!kWide) {   // wide lanes have one head
+                                        float b0 = c0 * u1 * f1.x, b1 = c1 * u1 * f1.y;
+                                        if (j0 == lim && own) b0 += dd1;
+                                        if (j1 == lim && own) b1 += dd1;
+                                        pk1[q] = pack_bf16x2(b0, b1);
+                                    }
                                 }
                             } else {
                                 mask_chunk_exact(R_cb + lane_off + m * 32, cs0, cs1, cj0, cj1,
@@ -749,20 +782,21 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                             }
                         }
                         tmem_st16(R_cb + lane_off + m * 32, pk0);
-                        tmem_st16(R_cb + lane_off + m * 32 + 16, pk1);
+                        if (!kWide) tmem_st16(R_cb + lane_off + m * 32 + 16, pk1);
                     }
-                    const float e = __expf(h == 0 ? cs0 : cs1);
-                    uint32_t v[32], u[32];
-                    tmem_ld32(R_acc + lane_off + h * 64, v);
-                    tmem_ld32(R_acc + lane_off + h * 64 + 32, u);
-                    tmem_ld_wait();
+                    // acc_h *= exp(cs_h[i]): narrow, head h's 64 columns; wide,
+                    // columns [32 h, 32 h + 32) of the one head
+                    const float e = __expf(h == 0 || kWide ? cs0 : cs1);
+#pragma unroll 1
+                    for (int half = 0; half < (kWide ? 1 : 2); ++half) {
+                        const uint32_t col = kWide ? 32 * h : 64 * h + 32 * half;
+                        uint32_t v[32];
+                        tmem_ld32(R_acc + lane_off + col, v);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        v[q] = __float_as_uint(__uint_as_float(v[q]) * e);
-                        u[q] = __float_as_uint(__uint_as_float(u[q]) * e);
+                        for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * e);
+                        tmem_st32(R_acc + lane_off + col, v);
                     }
-                    tmem_st32(R_acc + lane_off + h * 64, v);
-                    tmem_st32(R_acc + lane_off + h * 64 + 32, u);
                     tmem_st_wait();
                 }
                 tc_fence_before();
@@ -774,7 +808,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             } else if (k >= 1) {
                 // after the last block: the last y store has read its half of Xw
                 if (t == 0 && pend_store) tma_store_wait_read0();
-                named_bar(bar_wg, 128);
+                if (kWide) named_bar(3, 256); else named_bar(bar_wg, 128);
             }
 
             // (c) epilogue of the previous block: acc (TMEM) -> bf16 -> this
@@ -784,21 +818,23 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 const int ps = kk & 1;
                 fwait(&sm->mx_done[ps], (kk >> 1) & 1, a.status);
                 tc_fence_after();
-                const uint32_t R_prev = tbase + 256 + 128 * ps;
+                const uint32_t R_prev = tbase + 256 + Gm::ACC * ps;
                 // how y leaves the chip: 0 no valid head here, 1 TMA store of
                 // the whole tile, 2 direct stores of the rows inside the sequence
                 const BDesc &dp = sm->desc[kk % kDescRing];
-                const bool hvp = h < dp.nh;
+                const bool hvp = hs < dp.nh;
                 const int prev_mode = !hvp ? 0 : (dp.flags & kTmaY) ? 1 : 2;
-                const int prev_head = dp.h0 + (hvp ? h : 0);
+                const int prev_head = dp.h0 + (hvp ? hs : 0);
                 const int64_t prev_y =
                     (hvp && t < dp.rem) ? (((int64_t)dp.row * a.L + dp.tok + t) * a.H + prev_head) * kP : -1;
-                uint8_t *stile = sXw + (size_t)h * kT16;
+                uint8_t *stile = sXw + (size_t)hs * kT16;
                 uint8_t *srow = stile + t * 128;
+                // narrow: head h's 64 columns in two halves; wide: half h of
+                // the one head's row
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int half = kWide ? h : 0; half < (kWide ? h + 1 : 2); ++half) {
                     uint32_t v[32];
-                    tmem_ld32(R_prev + lane_off + h * 64 + half * 32, v);
+                    tmem_ld32(R_prev + lane_off + (kWide ? 0 : h * 64) + half * 32, v);
                     tmem_ld_wait();
                     uint4 pk[4];
 #pragma unroll
@@ -821,8 +857,8 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 tc_fence_before();
                 mbar_arrive(&sm->acc_free[ps]);
                 if (prev_mode == 1) fence_proxy_async_smem();
-                named_bar(bar_wg, 128);
-                if (t == 0 && prev_mode == 1) {
+                if (kWide) named_bar(3, 256); else named_bar(bar_wg, 128);
+                if (t == 0 && (!kWide || h == 0) && prev_mode == 1) {
                     tma_store_4d(&tmY, stile, 0, prev_head, dp.tok, dp.row);
                     tma_store_commit();
                     pend_store = true;
@@ -834,15 +870,16 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             const BDesc &dk = sm->desc[k % kDescRing];
             const int flags = dk.flags;
             if (flags & kSegEnd) {
-                const bool hv = h < dk.nh;
-                const int head = dk.h0 + (hv ? h : 0);
+                const bool hv = hs < dk.nh;
+                const int head = dk.h0 + (hv ? hs : 0);
                 const bool fin = (flags & kFin) != 0;
+                const int n_row = kWide ? 128 * h + t : t;   // this thread's state row
                 float *dst = nullptr;
                 if (fin) {
                     if (a.final_states && hv)
-                        dst = a.final_states + ((int64_t)dk.s * a.H + head) * kP * kN;
+                        dst = a.final_states + ((int64_t)dk.s * a.H + head) * kP * NS;
                 } else {
-                    dst = a.hslot + (size_t)ticket * kStateFloats + h * kP * kN;
+                    dst = a.hslot + (size_t)ticket * kStateFloats + hs * kP * NS;
                 }
 #pragma unroll 1
                 for (int c4 = 0; c4 < kP / 4; ++c4) {
@@ -852,7 +889,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     if (dst) {
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            __stcg(dst + (c4 * 4 + q) * kN + t, __uint_as_float(r[q]));
+                            __stcg(dst + (c4 * 4 + q) * NS + n_row, __uint_as_float(r[q]));
                     }
                 }
                 tc_fence_before();
@@ -970,9 +1007,12 @@ struct FLayout {
     int grid;
 };
 
-int64_t lanes_of(const Problem &p) {
-    const int hpg = p.H / p.G;
-    return (int64_t)p.nseq * p.G * ((hpg + 1) / 2);
+// Heads per lane: two of a group with dstate 128, one with dstate 256.
+int heads_per_lane(const Problem &p) { return p.N == 256 ? 1 : 2; }
+
+int64_t lanes_per_seq(const Problem &p) {
+    const int hpg = p.H / p.G, hpl = heads_per_lane(p);
+    return (int64_t)p.G * ((hpg + hpl - 1) / hpl);
 }
 
 // Grid: at most one CTA per SM, and never more CTAs than blocks (so that no
@@ -981,12 +1021,11 @@ int64_t lanes_of(const Problem &p) {
 // per SM, so its size does not depend on cu_seqlens.
 FLayout fused_layout(const Problem &p) {
     FLayout w{};
-    const int hpg = p.H / p.G;
-    const int64_t ptot = (int64_t)p.G * ((hpg + 1) / 2);
+    const int64_t ptot = lanes_per_seq(p);
     const int64_t sms = sm_count();
     int64_t grid;
     if (p.cu) grid = min64(sms, ptot * ((p.seqlen + kB - 1) / kB));
-    else grid = min64(sms, lanes_of(p));
+    else grid = min64(sms, (int64_t)p.nseq * ptot);
     w.grid = (int)max64(1, grid);
     size_t off = 0;
     w.hdr = off;     // ticket (4 B) + flags
@@ -1004,7 +1043,7 @@ FLayout fused_layout(const Problem &p) {
 size_t fused_workspace_bytes(const Problem &p) { return fused_layout(p).total; }
 
 int fused_supported(const Problem &p) {
-    if (p.dtype != SSD_BF16 || p.P != kP || p.N != kN) return SSD_ERR_UNSUPPORTED;
+    if (p.dtype != SSD_BF16 || p.P != kP || (p.N != 128 && p.N != 256)) return SSD_ERR_UNSUPPORTED;
     if (!encode_fn()) return SSD_ERR_UNSUPPORTED;
     return SSD_OK;
 }
@@ -1013,7 +1052,8 @@ cudaError_t fused_launch(const Problem &p) {
     const FLayout w = fused_layout(p);
     FArgs a{};
     a.L = p.seqlen;
-    a.H = p.H; a.G = p.G; a.hpg = p.H / p.G; a.npg = (a.hpg + 1) / 2; a.ptot = p.G * a.npg;
+    a.H = p.H; a.G = p.G; a.hpg = p.H / p.G; a.hpl = heads_per_lane(p);
+    a.npg = (a.hpg + a.hpl - 1) / a.hpl; a.ptot = p.G * a.npg;
     a.nseq = p.nseq;
     a.varlen = p.cu != nullptr;
     a.nb_fixed = (int)((p.seqlen + kB - 1) / kB);
@@ -1045,10 +1085,13 @@ cudaError_t fused_launch(const Problem &p) {
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    auto kern = a.dtt.on ? k_ssd_fused<true> : k_ssd_fused<false>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    const bool wide = p.N == 256;
+    auto kern = wide ? (a.dtt.on ? k_ssd_fused<true, true> : k_ssd_fused<false, true>)
+                     : (a.dtt.on ? k_ssd_fused<true, false> : k_ssd_fused<false, false>);
+    const size_t smem = wide ? smem_bytes<true>() : smem_bytes<false>();
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<w.grid, kThreads, kSmemBytes, p.stream>>>(tmX, tmB, tmC, tmY, a);
+    kern<<<w.grid, kThreads, smem, p.stream>>>(tmX, tmB, tmC, tmY, a);
     return cudaGetLastError();
 }
 

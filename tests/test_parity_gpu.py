@@ -271,3 +271,23 @@ def test_host_buffers_round_trip():
     y_ref, f_ref = oracle_full(inp)
     assert rel_err(y.float().numpy(), y_ref) <= TOL["bf16"]
     assert rel_err(fin.numpy(), f_ref) <= TOL["bf16"]
+
+
+# ---------------------------------------------------------------- wide lanes
+# dstate 256: the fused kernel runs one head per lane, the state's two
+# 128-row halves in the two warpgroups.
+
+@pytest.mark.parametrize("kw", [
+    dict(seed=41, batch=4, seqlen=400, nheads=64, init_states=True),    # 256 lanes > SMs: handoffs
+    dict(seed=42, batch=1, seqlen=130, nheads=8, init_states=False),    # one block and a 2-token tail
+])
+def test_wide_lanes_fused(kw):
+    inp = ssd_synth.make_inputs(W[3], **kw)
+    _compare_full(inp, "tc")
+
+
+@pytest.mark.parametrize("segs", [[300, 1, 0, 450, 249], [128] * 6])
+def test_wide_lanes_packed_sequences(segs):
+    inp = ssd_synth.make_inputs(W[3], seed=43, batch=1, seqlen=sum(segs), nheads=16,
+                                init_states=True, segment_lengths=segs)
+    _compare_full(inp, "tc")
