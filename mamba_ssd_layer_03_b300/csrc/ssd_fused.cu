@@ -313,6 +313,21 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+
+// Two fp32 products in one packed instruction (mul.rn.f32x2, IEEE round to
+// nearest in each half: the same results as two separate multiplies).
+__device__ __forceinline__ void mul2(uint32_t &a0, uint32_t &a1, float s0, float s1) {
+    asm("{\n .reg .b64 x, y;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %3};\n"
+        " mul.rn.f32x2 x, x, y;\n mov.b64 {%0, %1}, x;\n}"
+        : "+r"(a0), "+r"(a1)
+        : "r"(__float_as_uint(s0)), "r"(__float_as_uint(s1)));
+}
+__device__ __forceinline__ float2 mul2f(float2 a, float2 b) {
+    uint32_t x = __float_as_uint(a.x), y = __float_as_uint(a.y);
+    mul2(x, y, b.x, b.y);
+    return make_float2(__uint_as_float(x), __uint_as_float(y));
+}
+
 // TMEM column of k-step kk (tokens j in [16 kk, 16 kk + 16)) of the masked
 // block of head hh: M is written over C B^T in place, each 32-column fp32
 // chunk of C B^T (j in [32 m, 32 m + 32)) turning into the two heads'
@@ -677,8 +692,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                                 pack_bf16x2(__uint_as_float(v[half][8 * c + 4]), __uint_as_float(v[half][8 * c + 5])),
                                 pack_bf16x2(__uint_as_float(v[half][8 * c + 6]), __uint_as_float(v[half][8 * c + 7])));
 #pragma unroll
-                        for (int q = 0; q < 32; ++q)
-                            v[half][q] = __float_as_uint(decay * __uint_as_float(v[half][q]));
+                        for (int q = 0; q < 32; q += 2) mul2(v[half][q], v[half][q + 1], decay, decay);
                         tmem_st32(R_H + lane_off + h * 64 + half * 32, v[half]);
                     }
                 }
@@ -762,6 +776,22 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                                 tmem_ld_wait();
                                 const float u0 = __expf(cs0 - end0), u1 = __expf(cs1 - end1);
                                 const float *vf0 = vfs[0] + m * 32, *vf1 = vfs[1] + m * 32;
+                                if (!own) {
+                                    // a chunk wholly below the diagonal: no causal
+                                    // or diagonal test per element
+#pragma unroll
+                                    for (int q = 0; q < 16; ++q) {
+                                        const float2 f0 = *(const float2 *)(vf0 + 2 * q);
+                                        const float2 cc = make_float2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+                                        const float2 ca = mul2f(mul2f(cc, make_float2(u0, u0)), f0);
+                                        pk0[q] = pack_bf16x2(ca.x, ca.y);
+                                        if (!kWide) {
+                                            const float2 f1 = *(const float2 *)(vf1 + 2 * q);
+                                            const float2 cb = mul2f(mul2f(cc, make_float2(u1, u1)), f1);
+                                            pk1[q] = pack_bf16x2(cb.x, cb.y);
+                                        }
+                                    }
+                                } else
 #pragma unroll
                                 for (int q = 0; q < 16; ++q) {
                                     const int j0 = 2 * q, j1 = 2 * q + 1;
@@ -769,12 +799,14 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                                     const float c1 = (j1 <= lim) ? __uint_as_float(v[j1]) : 0.f;
                                     const float2 f0 = *(const float2 *)(vf0 + j0);
                                     const float2 f1 = *(const float2 *)(vf1 + j0);
-                                    float a0 = c0 * u0 * f0.x, a1 = c1 * u0 * f0.y;
+                                    const float2 ca = mul2f(mul2f(make_float2(c0, c1), make_float2(u0, u0)), f0);
+                                    float a0 = ca.x, a1 = ca.y;
                                     if (j0 == lim && own) a0 += dd0;
                                     if (j1 == lim && own) a1 += dd0;
                                     pk0[q] = pack_bf16x2(a0, a1);
                                     if (!kWide) {   // wide lanes have one head
-                                        float b0 = c0 * u1 * f1.x, b1 = c1 * u1 * f1.y;
+                                        const float2 cb = mul2f(mul2f(make_float2(c0, c1), make_float2(u1, u1)), f1);
+                                        float b0 = cb.x, b1 = cb.y;
                                         if (j0 == lim && own) b0 += dd1;
                                         if (j1 == lim && own) b1 += dd1;
                                         pk1[q] = pack_bf16x2(b0, b1);
@@ -799,7 +831,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                         tmem_ld32(R_acc + lane_off + col, v);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * e);
+                        for (int q = 0; q < 32; q += 2) mul2(v[q], v[q + 1], e, e);
                         tmem_st32(R_acc + lane_off + col, v);
                     }
                     tmem_st_wait();
