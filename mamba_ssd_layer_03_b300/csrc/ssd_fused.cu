@@ -1,5 +1,5 @@
 // Fused single-pass tensor-core path of the SSD forward scan (bf16 x/B/C/y,
-// fp32 dt/A/D/states, headdim 64, dstate 128).
+// fp32 dt/A/D/states, headdim 64, dstate 128 or 256).
 //
 // The scan is the block decomposition of the semiseparable matrix
 // M = L o (C B^T) (QbitAI article "新架构Mamba更新二代！", sections
@@ -7,16 +7,17 @@
 // products inside a block of tokens plus a linear recurrence of the per-head
 // state across blocks.  Here the recurrence never leaves the chip.
 //
-// Work decomposition.  A "lane" is one sequence and a pair of heads of the
-// same B/C group; its blocks are consecutive 128-token pieces of the
-// sequence.  All blocks of all lanes are numbered lane-major and every CTA
-// takes a contiguous range of that numbering (its "ticket" decides which),
+// Work decomposition.  A "lane" is one sequence and the heads it carries:
+// two heads of the same B/C group with dstate 128 (narrow lanes), one head
+// with dstate 256 (wide lanes).  Its blocks are consecutive 128-token pieces
+// of the sequence.  All blocks of all lanes are numbered lane-major and every
+// CTA takes a contiguous range of that numbering (its "ticket" decides which),
 // so the load is balanced to within one block.  A CTA walks its blocks in
-// order and keeps the running state of its lane in registers.  When a lane
-// is split between two CTAs, the earlier CTA hands the state at the split
-// point to the later one through global memory; every CTA processes the
-// lane it hands off first and the lane it receives last, so the receiver
-// rarely waits.
+// order and keeps the running state of its lane in TMEM.  When a lane is
+// split between two CTAs, the earlier CTA hands the state at the split point
+// to the later one through global memory; every CTA processes the lane it
+// hands off first and the lane it receives last, so the receiver rarely
+// waits.
 //
 // Per block (tokens i, j in [0, 128), heads h of the lane, state H_h[p][n]
 // at the block start, cs_h = within-block cumulative sum of dt*A_h):
@@ -24,23 +25,29 @@
 //   Ys_h = C H_h^T                                  tensor cores -> TMEM acc
 //   Xw_h = exp(cs_h[127] - cs_h[j]) dt_h[j] x_h[j]   CUDA cores, shared memory
 //   S_h  = B^T Xw_h                                 tensor cores -> TMEM
-//   H_h <- exp(cs_h[127]) H_h + S_h                 CUDA cores, registers
+//   H_h <- exp(cs_h[127]) H_h + S_h                 decay by CUDA cores in TMEM,
+//                                                   S accumulated by the MMA
 //   M_h  = CB o exp(cs_h[i] - cs_h[j]) dt_h[j] [j <= i] + D_h [i == j]
 //                                                   CUDA cores, TMEM (bf16)
 //   acc_h = exp(cs_h[i]) Ys_h + M_h x_h            tensor cores (A from TMEM)
-//   y_h  = acc_h                                    -> global (bf16)
+//   y_h  = acc_h                                    -> shared memory -> TMA store
 // Every exponent is <= 0.  Adding D_h on the diagonal of M_h folds the skip
 // term D_h x_h into the same product.  The masked block is factored at
 // 32-token sub-blocks: for j in an earlier sub-block with last token e,
 // exp(cs_i - cs_j) = exp(cs_i - cs_e) exp(cs_e - cs_j), so only the sub-block
 // holding i needs one exponential per element.
 //
-// Roles (320 threads, one CTA per SM): warps 0-3 and 4-7 are the two head
-// slots of the lane (TMEM lane = thread index within the warpgroup), warp 8
-// issues the TMA loads, warp 9 issues the MMAs.  They hand work to each
-// other through mbarriers; every wait is bounded in time and, once the
-// call's status word records an error, falls through so that the kernel
-// always finishes.
+// Roles (320 threads, one CTA per SM).  Warps 0-3 and 4-7 are two
+// warpgroups that each cover all 128 TMEM lanes (thread index within the
+// warpgroup = TMEM lane).  Narrow lanes: warpgroup h holds head h for the
+// scan, the state and y, and columns [64 h, 64 h + 64) of C B^T for the mask.
+// Wide lanes: both scan the one head; warpgroup h holds state rows
+// [128 h, 128 h + 128), half of each row of Xw and y, and the same column half
+// of C B^T.  Warp 8 issues the TMA loads and writes a descriptor of each block
+// (lane, tokens, flags, A, D) into a small shared-memory ring; warp 9 issues
+// the MMAs.  They hand work to each other through mbarriers; every wait is
+// bounded in time and, once the call's status word records an error, falls
+// through so that the kernel always finishes.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
