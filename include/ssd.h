@@ -227,6 +227,21 @@ SSD_API int ssd_step(const ssd_step_shape *shape, const void *x, const float *dt
  */
 SSD_API int ssd_check_device_status(const void *workspace, void *stream);
 
+/*
+ * Diagnostic of the failure path (not part of a scan).  Runs one of the fused
+ * kernel's bounded device-side waits where nothing will ever satisfy it:
+ * which = 0 waits on a shared-memory mbarrier that no thread or copy
+ * completes, which = 1 on a handoff flag (global memory) that no CTA sets.
+ * The wait gives up after its time limit (2 s), records the error in the
+ * status word and returns, so the context stays usable.
+ *   device_words  DEVICE pointer to 2 ints of scratch owned by the caller
+ *                 (status word, flag); cleared by the call
+ * Synchronises `stream`, then returns the status word the device recorded:
+ * SSD_ERR_DEVICE_TIMEOUT when the path works.  SSD_ERR_INVALID_ARG for a bad
+ * `which` or pointer, SSD_ERR_CUDA if a CUDA call failed.
+ */
+SSD_API int ssd_selftest_wait_timeout(int which, int *device_words, void *stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 SSD_API const char *ssd_status_string(int status);
 

@@ -105,6 +105,8 @@ def load_library() -> ctypes.CDLL:
     lib.ssd_scan_ex.restype = ctypes.c_int
     lib.ssd_step.argtypes = [ctypes.POINTER(SsdStepShape), vp, vp, tp, vp, vp, vp, vp, vp, vp, vp]
     lib.ssd_step.restype = ctypes.c_int
+    lib.ssd_selftest_wait_timeout.argtypes = [ctypes.c_int, vp, vp]
+    lib.ssd_selftest_wait_timeout.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -303,6 +305,17 @@ def ssd_step(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor
     if rc != 0:
         raise SsdError(rc, "ssd_step")
     return y
+
+
+def selftest_wait_timeout(which: int) -> int:
+    """Make one of the kernels' bounded waits run out on purpose (0: an
+    mbarrier nothing completes, 1: a handoff flag nothing sets) and return the
+    status the device recorded (5, SSD_ERR_DEVICE_TIMEOUT, when the failure
+    path works).  Takes about 2 s."""
+    words = torch.zeros(2, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    return int(load_library().ssd_selftest_wait_timeout(int(which), _ptr(words),
+                                                        ctypes.c_void_p(stream)))
 
 
 def _scan_from_host(x, dt, A, B, C, D, chunk_size, initial_states, cu_seqlens,

@@ -54,12 +54,14 @@
 
 #include "ssd_device.cuh"
 #include "ssd_internal.h"
+#include "ssd_wait.cuh"
 #include "tc_ptx.cuh"
 
 namespace ssd {
 namespace {
 
 using namespace tc;
+using namespace wait;
 typedef __nv_bfloat16 bf16;
 
 constexpr int kB = 128;                    // tokens per block
@@ -258,47 +260,6 @@ __device__ __forceinline__ void walk_next(const FArgs &a, Walk &w) {
 
 __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-__device__ __forceinline__ int ld_acquire_i(const int *p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release_i(int *p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// mbarrier.try_wait with a suspend-time hint: a waiting thread sleeps (and
-// issues nothing) until the phase completes or about `ns` have passed.
-__device__ __forceinline__ bool try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait.  Once it has waited far longer than any healthy step takes
-// (20 us), it also gives up as soon as the call's status word records an
-// error, so that a failed call finishes quickly; the status word is not read
-// before then because that global read would delay the wake-up.
-__device__ __forceinline__ bool fwait(uint64_t *bar, uint32_t parity, int *status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        for (int i = 0; i < 16; ++i)
-            if (try_wait_sleep(bar, parity, 2000)) return true;
-        const uint64_t dt = globaltimer_ns() - t0;
-        if (dt > 20000ull && status_bad(status)) return false;
-        if (dt > kWaitLimitNs) {
-            set_status(status, SSD_ERR_DEVICE_TIMEOUT);
-            return false;
-        }
-    }
 }
 
 // Plain bounded wait used only while draining at exit.
@@ -647,16 +608,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     const float *src = nullptr;
                     bool from_slot = false;
                     if (flags & kFromSlot) {
-                        const int *flag = a.hflag + (ticket - 1);
-                        const uint64_t tw = globaltimer_ns();
-                        while (ld_acquire_i(flag) == 0) {
-                            if (status_bad(a.status)) break;
-                            if (globaltimer_ns() - tw > kWaitLimitNs) {
-                                set_status(a.status, SSD_ERR_DEVICE_TIMEOUT);
-                                break;
-                            }
-                            __nanosleep(64);
-                        }
+                        wait_flag(a.hflag + (ticket - 1), a.status);
                         src = a.hslot + (size_t)(ticket - 1) * kStateFloats + hs * kP * NS;
                         from_slot = true;
                     } else if (a.init && hv) {

@@ -195,3 +195,10 @@ def test_step_zero_batch_is_a_no_op():
     sh = _step_shape(batch=0)
     assert lib.ssd_step(ctypes.byref(sh), None, None, None, None, None, None, None, None, None,
                         None) == 0
+
+
+def test_selftest_rejects_bad_arguments():
+    lib = ssd.load_library()
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.ssd_selftest_wait_timeout(2, fake, None) == 1
+    assert lib.ssd_selftest_wait_timeout(0, None, None) == 1
