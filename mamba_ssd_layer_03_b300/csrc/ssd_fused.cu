@@ -98,6 +98,13 @@ struct FArgs {
     float *hslot;              // [grid][2][P][N] handoff states
     const int *seqblk;         // [nseq + 1] prefix of blocks per sequence (varlen)
     DtTransform dtt;           // step-size transform applied as dt is read
+    // Few-lane workloads split lanes between CTAs and run twice (see the
+    // kernel's kPre): per ticket, the log of the decay over its part of the
+    // lane it hands off, [grid][2]; and the main run's flag to fold the state
+    // at a split from those records instead of waiting for a handoff.
+    float *logdec;
+    float *hstart;             // [grid][state]: folded start state of each split (main run)
+    int chain;
 };
 
 // One block of a CTA's walk as the compute warps need it, written by the TMA
@@ -356,7 +363,13 @@ __device__ __noinline__ void mask_chunk_exact(uint32_t taddr, float cs0, float c
 
 // kDtTransform: the step-size transform is compiled in only where a call asks
 // for it, so the plain scan carries no trace of it.
-template <bool kDtTransform, bool kWide>
+// kPre: the state-only first run of a few-lane workload.  Each CTA runs
+// its range from a zero state where a lane began in an earlier CTA, skips
+// everything that only y needs (C, C B^T, C H^T, the mask, M x, the epilogue)
+// and records, where its range splits a lane, that partial state and the log
+// of its decay.  The second run (kPre false, chain set) starts each split
+// lane from those records instead of waiting for the previous CTA.
+template <bool kDtTransform, bool kWide, bool kPre>
 __global__ void __launch_bounds__(kThreads, 1)
 k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmY,
@@ -410,8 +423,9 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 {
                     // slot k % 4 last described block k - 4: the compute warps
                     // were done with it (its epilogue included) before they
-                    // made block k - 2's H operand ready, which the c_empty
-                    // completion waited for in the previous iteration follows
+                    // made block k - 2's H operand and Xw ready, which the
+                    // c_empty and b_empty completions waited for in the
+                    // previous iteration follow
                     BDesc &d = sm->desc[k % kDescRing];
                     const Lane &ln = w.ln;
                     const int i0 = w.b * kB;
@@ -438,10 +452,12 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     tma_load_4d(sX + (size_t)(slot * HL + s) * kT16, &tmX, &sm->x_full[slot], 0,
                                 w.ln.h0 + s, tok, w.ln.row);
                 mbar_arrive_expect_tx(&sm->x_full[slot], HL * kT16);
-                if (k >= 1) fwait(&sm->c_empty, (k - 1) & 1, a.status);
-                for (int nb = 0; nb < NA; ++nb)
-                    tma_load_4d(sC + nb * kT16, &tmC, &sm->c_full, nb * 64, w.ln.g, tok, w.ln.row);
-                mbar_arrive_expect_tx(&sm->c_full, NA * kT16);
+                if (!kPre) {
+                    if (k >= 1) fwait(&sm->c_empty, (k - 1) & 1, a.status);
+                    for (int nb = 0; nb < NA; ++nb)
+                        tma_load_4d(sC + nb * kT16, &tmC, &sm->c_full, nb * 64, w.ln.g, tok, w.ln.row);
+                    mbar_arrive_expect_tx(&sm->c_full, NA * kT16);
+                }
                 if (k >= 1) fwait(&sm->b_empty, (k - 1) & 1, a.status);
                 for (int nb = 0; nb < NA; ++nb)
                     tma_load_4d(sB + nb * kT16, &tmB, &sm->b_full, nb * 64, w.ln.g, tok, w.ln.row);
@@ -449,7 +465,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             }
             // let every copy this thread started land before the CTA exits
             if (k >= 1) {
-                drain_wait(&sm->c_full, (k - 1) & 1);
+                if (!kPre) drain_wait(&sm->c_full, (k - 1) & 1);
                 drain_wait(&sm->b_full, (k - 1) & 1);
                 drain_wait(&sm->x_full[(k - 1) & 1], ((k - 1) >> 1) & 1);
             }
@@ -469,9 +485,26 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             for (uint32_t k = 0; k < nblk; ++k) {
                 const int slot = k & 1;
                 const uint32_t R_acc = tbase + 256 + Gm::ACC * slot;
-                fwait(&sm->c_full, k & 1, a.status);
+                if (!kPre) fwait(&sm->c_full, k & 1, a.status);
                 fwait(&sm->b_full, k & 1, a.status);
                 tc_fence_after();
+                if (kPre) {
+                    // state only: H <- (decay H, in TMEM once hop_ready) + B^T Xw
+                    fwait(&sm->hop_ready, k & 1, a.status);
+                    fwait(&sm->xw_ready, k & 1, a.status);
+                    tc_fence_after();
+#pragma unroll
+                    for (int q = 0; q < (kWide ? 2 : 1); ++q)
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_ss(R_H + 64 * q,
+                                   smem_desc(sbb + 2 * q * kT16 + kk * 2048, kT16, 1024, kSwizzle128B),
+                                   smem_desc(sxw + kk * 2048, kT16, 1024, kSwizzle128B), id_s, 1);
+                    mma_commit(&sm->s_done);
+                    mma_commit(&sm->b_empty);
+                    mma_commit(&sm->x_empty[slot]);   // x was read by Xw, before xw_ready
+                    continue;
+                }
                 // CB = C B^T (over the previous block's M, read by its last product)
 #pragma unroll
                 for (int kk = 0; kk < 4 * NA; ++kk) {
@@ -559,6 +592,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         };
         bool have_next = false;
         bool pend_store = false;   // a TMA store of y still reads this half of Xw
+        float ldsum = 0.f;         // pre run: sum of cs_last over the lane's blocks here
         const uint32_t nblk = (uint32_t)cta_blocks(a, ticket);
 
         for (uint32_t k = 0;; ++k) {
@@ -594,9 +628,11 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 incl += (wq > 0 ? p0 : 0.f) + (wq > 1 ? p1 : 0.f) + (wq > 2 ? p2 : 0.f);
                 const float cs_last = ((p0 + p1) + p2) + p3;
                 const float sub_end = __shfl_sync(0xffffffffu, incl, 31);
-                sm->cs[slot][h][t] = incl;
-                sm->dtv[slot][h][t] = d;
-                sm->vf[slot][h][t] = __expf(sub_end - incl) * d;
+                if (!kPre) {   // for the mask
+                    sm->cs[slot][h][t] = incl;
+                    sm->dtv[slot][h][t] = d;
+                    sm->vf[slot][h][t] = __expf(sub_end - incl) * d;
+                }
                 const float w_t = __expf(fminf(cs_last - incl, 0.f)) * d;
                 const float decay = __expf(cs_last);
 
@@ -604,18 +640,31 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 //     TMEM, ready for the S product to accumulate on.  A lane's
                 //     first block takes H_k from the initial state (or the
                 //     previous CTA's handoff) through TMEM.
+                if (kPre && seg_start) ldsum = 0.f;
+                if (kPre) ldsum += cs_last;
                 if (seg_start) {
+                    // A lane split at this CTA's range start begins from: zero
+                    // (pre run); the fold of the earlier CTAs' pre-run records
+                    // (main run of a few-lane workload); or the previous CTA's
+                    // handoff.
                     const float *src = nullptr;
                     bool from_slot = false;
+                    const int n_row = kWide ? 128 * h + t : t;   // this thread's state row
                     if (flags & kFromSlot) {
-                        wait_flag(a.hflag + (ticket - 1), a.status);
-                        src = a.hslot + (size_t)(ticket - 1) * kStateFloats + hs * kP * NS;
-                        from_slot = true;
+                        if (kPre) {
+                        } else if (a.chain) {
+                            // folded from the pre run's records between the runs
+                            src = a.hstart + (size_t)ticket * kStateFloats + hs * kP * NS;
+                            from_slot = true;
+                        } else {
+                            wait_flag(a.hflag + (ticket - 1), a.status);
+                            src = a.hslot + (size_t)(ticket - 1) * kStateFloats + hs * kP * NS;
+                            from_slot = true;
+                        }
                     } else if (a.init && hv) {
                         src = a.init + ((int64_t)dk.s * a.H + head) * kP * NS;
                     }
                     if (!hv) src = nullptr;
-                    const int n_row = kWide ? 128 * h + t : t;   // this thread's state row
 #pragma unroll 1
                     for (int c4 = 0; c4 < kP / 4; ++c4) {
                         uint32_t r[4];
@@ -645,7 +694,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     for (int half = 0; half < 2; ++half) {
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
-                            *(uint4 *)(hrow + (((half * 4 + c) ^ (t & 7)) << 4)) = make_uint4(
+                            if (!kPre) *(uint4 *)(hrow + (((half * 4 + c) ^ (t & 7)) << 4)) = make_uint4(
                                 pack_bf16x2(__uint_as_float(v[half][8 * c]), __uint_as_float(v[half][8 * c + 1])),
                                 pack_bf16x2(__uint_as_float(v[half][8 * c + 2]), __uint_as_float(v[half][8 * c + 3])),
                                 pack_bf16x2(__uint_as_float(v[half][8 * c + 4]), __uint_as_float(v[half][8 * c + 5])),
@@ -694,6 +743,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 tc_fence_before();
                 mbar_arrive(&sm->xw_ready);
 
+                if (!kPre) {   // everything below only serves y
                 // (e) masked block, in place over C B^T: this warpgroup turns
                 //     columns j in [64 h, 64 h + 64) into both heads' M pieces;
                 //     then acc_h *= exp(cs_h[i]) for head h
@@ -801,7 +851,8 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 // the S product of this block has read Xw once s_done completes
                 fwait(&sm->s_done, k & 1, a.status);
                 tc_fence_after();
-            } else if (k >= 1) {
+                }
+            } else if (!kPre && k >= 1) {
                 // after the last block: the last y store has read its half of Xw
                 if (t == 0 && pend_store) tma_store_wait_read0();
                 if (kWide) named_bar(3, 256); else named_bar(bar_wg, 128);
@@ -809,7 +860,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 
             // (c) epilogue of the previous block: acc (TMEM) -> bf16 -> this
             //     head's half of Xw -> TMA store
-            if (k >= 1) {
+            if (!kPre && k >= 1) {
                 const uint32_t kk = k - 1;
                 const int ps = kk & 1;
                 fwait(&sm->mx_done[ps], (kk >> 1) & 1, a.status);
@@ -870,12 +921,16 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 const int head = dk.h0 + (hv ? hs : 0);
                 const bool fin = (flags & kFin) != 0;
                 const int n_row = kWide ? 128 * h + t : t;   // this thread's state row
+                if (kPre) fwait(&sm->s_done, k & 1, a.status);   // (the main run waits below)
                 float *dst = nullptr;
                 if (fin) {
-                    if (a.final_states && hv)
+                    // the pre run leaves final states to the main run
+                    if (!kPre && a.final_states && hv)
                         dst = a.final_states + ((int64_t)dk.s * a.H + head) * kP * NS;
-                } else {
+                } else if (kPre || !a.chain) {
+                    // handoff (pre run: the record the main run folds)
                     dst = a.hslot + (size_t)ticket * kStateFloats + hs * kP * NS;
+                    if (kPre && t == 0 && (!kWide || h == 0)) a.logdec[2 * ticket + hs] = ldsum;
                 }
 #pragma unroll 1
                 for (int c4 = 0; c4 < kP / 4; ++c4) {
@@ -903,6 +958,31 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+// Between the two runs of a few-lane workload: for every CTA whose range
+// begins inside a lane, its start state.  Ticket u0's range holds the lane's
+// first block, so its pre-run record is the whole state up to its range end;
+// every later ticket u before this one adds H <- exp(logdec_u) H + S_u.
+// One CTA per ticket, threads over the state's values.
+__global__ void k_fused_chain_fold(FArgs a, int NS) {
+    if (status_bad(a.status)) return;
+    const int ticket = blockIdx.x;
+    const int64_t T = total_blocks(a);
+    const int64_t g0 = (int64_t)ticket * T / a.grid;
+    if (ticket == 0 || g0 >= T) return;
+    const Lane ln = lane_info(a, find_lane(a, g0));
+    if (ln.start >= g0) return;      // the range begins at a lane start
+    int u0 = ticket - 1;
+    while (u0 > 0 && (int64_t)u0 * T / a.grid > ln.start) --u0;
+    for (int e = threadIdx.x; e < kStateFloats; e += blockDim.x) {
+        const int hs = e / (kP * NS);
+        float hv = __ldcg(a.hslot + (size_t)u0 * kStateFloats + e);
+        for (int u = u0 + 1; u < ticket; ++u)
+            hv = fmaf(__expf(__ldcg(a.logdec + 2 * u + hs)), hv,
+                      __ldcg(a.hslot + (size_t)u * kStateFloats + e));
+        a.hstart[(size_t)ticket * kStateFloats + e] = hv;
+    }
 }
 
 // Varlen set-up: blocks per sequence (exclusive prefix) and the final states
@@ -998,9 +1078,17 @@ int sm_count() {
     return n > 0 ? n : 148;
 }
 
+// Fewest blocks per CTA for which splitting lanes between CTAs pays.  The
+// state-only pre run costs about 0.7 of a full run per block (its per-block
+// latency chain stays), so a split with B blocks per CTA takes ~1.7 B block
+// times against a whole lane's; with 8 per CTA the small b2 x 12-pair layer
+// (16 blocks per lane) measured 82 us split against 72 us whole.
+constexpr int64_t kChainMinBlocks = 16;
+
 struct FLayout {
-    size_t hdr, slots, seqblk, total;
+    size_t hdr, slots, logdec, hstart, seqblk, total;
     int grid;
+    bool chain;   // few lanes: split them between CTAs, pre run + main run
 };
 
 // Heads per lane: two of a group with dstate 128, one with dstate 256.
@@ -1019,14 +1107,30 @@ FLayout fused_layout(const Problem &p) {
     FLayout w{};
     const int64_t ptot = lanes_per_seq(p);
     const int64_t sms = sm_count();
+    const int64_t nb = (p.seqlen + kB - 1) / kB;
     int64_t grid;
-    if (p.cu) grid = min64(sms, ptot * ((p.seqlen + kB - 1) / kB));
-    else grid = min64(sms, (int64_t)p.nseq * ptot);
+    if (p.cu) {
+        grid = min64(sms, ptot * nb);
+    } else if ((int64_t)p.nseq * ptot * 2 <= min64(sms, (int64_t)p.nseq * ptot * nb / kChainMinBlocks)) {
+        // At most half as many lanes as CTAs could take at kChainMinBlocks
+        // blocks each: lanes are split between CTAs, which start from the
+        // pre run's records.  Below that many blocks per CTA the second run
+        // and the per-split start and end cost more than the parallelism
+        // gains.
+        grid = min64(sms, (int64_t)p.nseq * ptot * nb / kChainMinBlocks);
+        w.chain = true;
+    } else {
+        grid = min64(sms, (int64_t)p.nseq * ptot);
+    }
     w.grid = (int)max64(1, grid);
     size_t off = 0;
     w.hdr = off;     // ticket (4 B) + flags
     off = align_up(off + 256 + (size_t)sms * sizeof(int), 256);
     w.slots = off;
+    off = align_up(off + (size_t)sms * kStateFloats * sizeof(float), 256);
+    w.logdec = off;
+    off = align_up(off + (size_t)sms * 2 * sizeof(float), 256);
+    w.hstart = off;
     off = align_up(off + (size_t)sms * kStateFloats * sizeof(float), 256);
     w.seqblk = off;
     off = align_up(off + (size_t)(p.nseq + 1) * sizeof(int), 256);
@@ -1062,6 +1166,8 @@ cudaError_t fused_launch(const Problem &p) {
     a.ticket = (int *)(p.ws + w.hdr);
     a.hflag = (int *)(p.ws + w.hdr + 256);
     a.hslot = (float *)(p.ws + w.slots);
+    a.logdec = (float *)(p.ws + w.logdec);
+    a.hstart = (float *)(p.ws + w.hstart);
     a.seqblk = (const int *)(p.ws + w.seqblk);
 
     cudaError_t e = cudaMemsetAsync(p.ws + w.hdr, 0, w.slots - w.hdr, p.stream);
@@ -1082,9 +1188,33 @@ cudaError_t fused_launch(const Problem &p) {
         if (e != cudaSuccess) return e;
     }
     const bool wide = p.N == 256;
-    auto kern = wide ? (a.dtt.on ? k_ssd_fused<true, true> : k_ssd_fused<false, true>)
-                     : (a.dtt.on ? k_ssd_fused<true, false> : k_ssd_fused<false, false>);
     const size_t smem = wide ? smem_bytes<true>() : smem_bytes<false>();
+    using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, FArgs);
+    auto pick = [&](bool pre) -> Kern {
+        if (wide) {
+            if (pre) return a.dtt.on ? k_ssd_fused<true, true, true> : k_ssd_fused<false, true, true>;
+            return a.dtt.on ? k_ssd_fused<true, true, false> : k_ssd_fused<false, true, false>;
+        }
+        if (pre) return a.dtt.on ? k_ssd_fused<true, false, true> : k_ssd_fused<false, false, true>;
+        return a.dtt.on ? k_ssd_fused<true, false, false> : k_ssd_fused<false, false, false>;
+    };
+    if (w.chain) {
+        // pre run: the state records at every split; then the tickets start
+        // again from zero for the main run
+        Kern pre = pick(true);
+        e = cudaFuncSetAttribute(pre, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        pre<<<w.grid, kThreads, smem, p.stream>>>(tmX, tmB, tmC, tmY, a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        k_fused_chain_fold<<<w.grid, 256, 0, p.stream>>>(a, p.N);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        e = cudaMemsetAsync(p.ws + w.hdr, 0, w.slots - w.hdr, p.stream);
+        if (e != cudaSuccess) return e;
+        a.chain = 1;
+    }
+    Kern kern = pick(false);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<w.grid, kThreads, smem, p.stream>>>(tmX, tmB, tmC, tmY, a);

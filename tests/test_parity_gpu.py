@@ -291,3 +291,19 @@ def test_wide_lanes_packed_sequences(segs):
     inp = ssd_synth.make_inputs(W[3], seed=43, batch=1, seqlen=sum(segs), nheads=16,
                                 init_states=True, segment_lengths=segs)
     _compare_full(inp, "tc")
+
+
+# ---------------------------------------------------------------- split lanes
+# Fewer lanes than SMs with long sequences: the fused kernel splits every lane
+# between several CTAs.  A state-only first run records each CTA's partial
+# state and decay; the records are folded into each split's start state; the
+# second run produces y.
+
+@pytest.mark.parametrize("wi,kw", [
+    (1, dict(seed=61, batch=1, seqlen=8192, nheads=24, init_states=True)),   # 12 lanes, 4 CTAs each
+    (1, dict(seed=62, batch=1, seqlen=6000, nheads=6, init_states=True)),    # ranges straddle lanes
+    (3, dict(seed=63, batch=1, seqlen=8192, nheads=8, init_states=True)),    # wide lanes
+], ids=["narrow", "straddle", "wide"])
+def test_split_lanes_two_runs(wi, kw):
+    inp = ssd_synth.make_inputs(W[wi], **kw)
+    _compare_full(inp, "tc")
