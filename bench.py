@@ -440,7 +440,8 @@ def main():
         }
         if args.seqlen is not None:
             out["config"]["seqlen_override"] = args.seqlen
-        out["gpu_launches"] = launches_per_step(algo, inp) * args.steps
+        out["gpu_launches"] = launches_per_step(
+            algo, inp, torch.cuda.get_device_properties(dev).multi_processor_count) * args.steps
         print(json.dumps(out))
     if dist:
         dist.destroy_process_group()
@@ -595,14 +596,26 @@ def run_step_bench(args, w, rank, world, local):
         dist.destroy_process_group()
 
 
-def launches_per_step(algo, inp):
+def fused_splits_lanes(inp, sms):
+    """Whether the fused kernel splits lanes between CTAs (its two-run mode):
+    at most half as many lanes as CTAs at 16 blocks each, no packing."""
+    if inp["cu_seqlens"] is not None:
+        return False
+    hpl = 1 if inp["dstate"] == 256 else 2
+    hpg = inp["nheads"] // inp["ngroups"]
+    lanes = inp["nseq"] * inp["ngroups"] * ((hpg + hpl - 1) // hpl)
+    nb = (inp["seqlen"] + 127) // 128
+    return lanes * 2 <= min(sms, lanes * nb // 16)
+
+
+def launches_per_step(algo, inp, sms=148):
     """Kernels libssd launches per ssd_scan() (memset of the status word is
     a copy-engine op, not a kernel)."""
     varlen = inp["cu_seqlens"] is not None
     if algo == "simt":
         return 4 + (2 if varlen else 0)
-    if algo == "tc":       # fused kernel (+ cu_seqlens check and set-up)
-        return 1 + (2 if varlen else 0)
+    if algo == "tc":       # fused kernel (+ cu_seqlens check and set-up; + pre run and fold)
+        return 1 + (2 if varlen else 0) + (2 if fused_splits_lanes(inp, sms) else 0)
     return 2
 
 

@@ -964,10 +964,15 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 // begins inside a lane, its start state.  Ticket u0's range holds the lane's
 // first block, so its pre-run record is the whole state up to its range end;
 // every later ticket u before this one adds H <- exp(logdec_u) H + S_u.
-// One CTA per ticket, threads over the state's values.
-__global__ void k_fused_chain_fold(FArgs a, int NS) {
+// Grid: y over the tickets, x over 1024-value slices of the state, one float4
+// per thread, so that every thread has its whole chain of loads in flight
+// (a CTA per ticket looping over the state ran latency-bound).
+constexpr int kFoldThreads = 256;
+constexpr int kFoldSlices = kStateFloats / (4 * kFoldThreads);
+static_assert(kStateFloats % (4 * kFoldThreads) == 0, "fold slices");
+__global__ void __launch_bounds__(kFoldThreads) k_fused_chain_fold(FArgs a, int NS) {
     if (status_bad(a.status)) return;
-    const int ticket = blockIdx.x;
+    const int ticket = blockIdx.y;
     const int64_t T = total_blocks(a);
     const int64_t g0 = (int64_t)ticket * T / a.grid;
     if (ticket == 0 || g0 >= T) return;
@@ -975,14 +980,18 @@ __global__ void k_fused_chain_fold(FArgs a, int NS) {
     if (ln.start >= g0) return;      // the range begins at a lane start
     int u0 = ticket - 1;
     while (u0 > 0 && (int64_t)u0 * T / a.grid > ln.start) --u0;
-    for (int e = threadIdx.x; e < kStateFloats; e += blockDim.x) {
-        const int hs = e / (kP * NS);
-        float hv = __ldcg(a.hslot + (size_t)u0 * kStateFloats + e);
-        for (int u = u0 + 1; u < ticket; ++u)
-            hv = fmaf(__expf(__ldcg(a.logdec + 2 * u + hs)), hv,
-                      __ldcg(a.hslot + (size_t)u * kStateFloats + e));
-        a.hstart[(size_t)ticket * kStateFloats + e] = hv;
+    const int e = 4 * (blockIdx.x * kFoldThreads + threadIdx.x);
+    const int hs = e / (kP * NS);
+    float4 hv = __ldcg(reinterpret_cast<const float4 *>(a.hslot + (size_t)u0 * kStateFloats + e));
+    for (int u = u0 + 1; u < ticket; ++u) {
+        const float d = __expf(__ldcg(a.logdec + 2 * u + hs));
+        const float4 s = __ldcg(reinterpret_cast<const float4 *>(a.hslot + (size_t)u * kStateFloats + e));
+        hv.x = fmaf(d, hv.x, s.x);
+        hv.y = fmaf(d, hv.y, s.y);
+        hv.z = fmaf(d, hv.z, s.z);
+        hv.w = fmaf(d, hv.w, s.w);
     }
+    *reinterpret_cast<float4 *>(a.hstart + (size_t)ticket * kStateFloats + e) = hv;
 }
 
 // Varlen set-up: blocks per sequence (exclusive prefix) and the final states
@@ -1207,7 +1216,7 @@ cudaError_t fused_launch(const Problem &p) {
         pre<<<w.grid, kThreads, smem, p.stream>>>(tmX, tmB, tmC, tmY, a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        k_fused_chain_fold<<<w.grid, 256, 0, p.stream>>>(a, p.N);
+        k_fused_chain_fold<<<dim3(kFoldSlices, w.grid), kFoldThreads, 0, p.stream>>>(a, p.N);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         e = cudaMemsetAsync(p.ws + w.hdr, 0, w.slots - w.hdr, p.stream);
