@@ -458,18 +458,35 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                         tma_load_4d(sC + nb * kT16, &tmC, &sm->c_full, nb * 64, w.ln.g, tok, w.ln.row);
                     mbar_arrive_expect_tx(&sm->c_full, NA * kT16);
                 }
-                if (k >= 1) fwait(&sm->b_empty, (k - 1) & 1, a.status);
-                for (int nb = 0; nb < NA; ++nb)
-                    tma_load_4d(sB + nb * kT16, &tmB, &sm->b_full, nb * 64, w.ln.g, tok, w.ln.row);
-                mbar_arrive_expect_tx(&sm->b_full, NA * kT16);
+                if (kPre) {
+                    // the pre run loads no C: B takes two slots, the second in
+                    // C's tiles with C's barriers, and is fetched a block ahead
+                    uint64_t *bf = slot ? &sm->c_full : &sm->b_full;
+                    if (k >= 2) fwait(slot ? &sm->c_empty : &sm->b_empty, ((k >> 1) + 1) & 1, a.status);
+                    for (int nb = 0; nb < NA; ++nb)
+                        tma_load_4d((slot ? sC : sB) + nb * kT16, &tmB, bf, nb * 64, w.ln.g, tok, w.ln.row);
+                    mbar_arrive_expect_tx(bf, NA * kT16);
+                } else {
+                    if (k >= 1) fwait(&sm->b_empty, (k - 1) & 1, a.status);
+                    for (int nb = 0; nb < NA; ++nb)
+                        tma_load_4d(sB + nb * kT16, &tmB, &sm->b_full, nb * 64, w.ln.g, tok, w.ln.row);
+                    mbar_arrive_expect_tx(&sm->b_full, NA * kT16);
+                }
             }
             // let every copy this thread started land before the CTA exits
             if (k >= 1) {
-                if (!kPre) drain_wait(&sm->c_full, (k - 1) & 1);
-                drain_wait(&sm->b_full, (k - 1) & 1);
+                if (kPre) {
+                    drain_wait((k - 1) & 1 ? &sm->c_full : &sm->b_full, ((k - 1) >> 1) & 1);
+                } else {
+                    drain_wait(&sm->c_full, (k - 1) & 1);
+                    drain_wait(&sm->b_full, (k - 1) & 1);
+                }
                 drain_wait(&sm->x_full[(k - 1) & 1], ((k - 1) >> 1) & 1);
             }
-            if (k >= 2) drain_wait(&sm->x_full[k & 1], ((k - 2) >> 1) & 1);
+            if (k >= 2) {
+                if (kPre) drain_wait(k & 1 ? &sm->c_full : &sm->b_full, ((k - 2) >> 1) & 1);
+                drain_wait(&sm->x_full[k & 1], ((k - 2) >> 1) & 1);
+            }
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA
@@ -485,11 +502,11 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             for (uint32_t k = 0; k < nblk; ++k) {
                 const int slot = k & 1;
                 const uint32_t R_acc = tbase + 256 + Gm::ACC * slot;
-                if (!kPre) fwait(&sm->c_full, k & 1, a.status);
-                fwait(&sm->b_full, k & 1, a.status);
-                tc_fence_after();
                 if (kPre) {
-                    // state only: H <- (decay H, in TMEM once hop_ready) + B^T Xw
+                    // state only: H <- (decay H, in TMEM once hop_ready) + B^T Xw,
+                    // B from its slot (the second one in C's tiles)
+                    fwait(slot ? &sm->c_full : &sm->b_full, (k >> 1) & 1, a.status);
+                    const uint32_t sbs = slot ? sc : sbb;
                     fwait(&sm->hop_ready, k & 1, a.status);
                     fwait(&sm->xw_ready, k & 1, a.status);
                     tc_fence_after();
@@ -498,13 +515,16 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
                             mma_ss(R_H + 64 * q,
-                                   smem_desc(sbb + 2 * q * kT16 + kk * 2048, kT16, 1024, kSwizzle128B),
+                                   smem_desc(sbs + 2 * q * kT16 + kk * 2048, kT16, 1024, kSwizzle128B),
                                    smem_desc(sxw + kk * 2048, kT16, 1024, kSwizzle128B), id_s, 1);
                     mma_commit(&sm->s_done);
-                    mma_commit(&sm->b_empty);
+                    mma_commit(slot ? &sm->c_empty : &sm->b_empty);
                     mma_commit(&sm->x_empty[slot]);   // x was read by Xw, before xw_ready
                     continue;
                 }
+                fwait(&sm->c_full, k & 1, a.status);
+                fwait(&sm->b_full, k & 1, a.status);
+                tc_fence_after();
                 // CB = C B^T (over the previous block's M, read by its last product)
 #pragma unroll
                 for (int kk = 0; kk < 4 * NA; ++kk) {
