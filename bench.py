@@ -598,14 +598,15 @@ def run_step_bench(args, w, rank, world, local):
 
 def fused_splits_lanes(inp, sms):
     """Whether the fused kernel splits lanes between CTAs (its two-run mode):
-    at most half as many lanes as CTAs at 16 blocks each, no packing."""
+    at most half as many lanes as SMs, at least 16 blocks per lane, no
+    packing."""
     if inp["cu_seqlens"] is not None:
         return False
     hpl = 1 if inp["dstate"] == 256 else 2
     hpg = inp["nheads"] // inp["ngroups"]
     lanes = inp["nseq"] * inp["ngroups"] * ((hpg + hpl - 1) // hpl)
     nb = (inp["seqlen"] + 127) // 128
-    return lanes * 2 <= min(sms, lanes * nb // 16)
+    return lanes * 2 <= sms and nb >= 16
 
 
 def launches_per_step(algo, inp, sms=148):

@@ -668,36 +668,36 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     // (main run of a few-lane workload); or the previous CTA's
                     // handoff.
                     const float *src = nullptr;
-                    bool from_slot = false;
                     const int n_row = kWide ? 128 * h + t : t;   // this thread's state row
                     if (flags & kFromSlot) {
                         if (kPre) {
                         } else if (a.chain) {
                             // folded from the pre run's records between the runs
                             src = a.hstart + (size_t)ticket * kStateFloats + hs * kP * NS;
-                            from_slot = true;
                         } else {
                             wait_flag(a.hflag + (ticket - 1), a.status);
                             src = a.hslot + (size_t)(ticket - 1) * kStateFloats + hs * kP * NS;
-                            from_slot = true;
                         }
                     } else if (a.init && hv) {
                         src = a.init + ((int64_t)dk.s * a.H + head) * kP * NS;
                     }
                     if (!hv) src = nullptr;
-#pragma unroll 1
-                    for (int c4 = 0; c4 < kP / 4; ++c4) {
-                        uint32_t r[4];
+                    // 16 loads in flight per round: the state's 64 columns
+                    // arrive in a few memory latencies, not sixteen
+                    if (src) {
+                        for (int c16 = 0; c16 < kP / 16; ++c16) {
+                            uint32_t r[16];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            float e = 0.f;
-                            if (src) {
-                                const float *sp = src + (c4 * 4 + q) * NS + n_row;
-                                e = from_slot ? __ldcg(sp) : __ldg(sp);
-                            }
-                            r[q] = __float_as_uint(e);
+                            for (int q = 0; q < 16; ++q)
+                                r[q] = __float_as_uint(__ldcg(src + (c16 * 16 + q) * NS + n_row));
+                            tmem_st16(R_H + lane_off + h * 64 + c16 * 16, r);
                         }
-                        tmem_st4(R_H + lane_off + h * 64 + c4 * 4, r);
+                    } else {
+                        uint32_t r[16];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) r[q] = 0u;
+#pragma unroll 1
+                        for (int c16 = 0; c16 < kP / 16; ++c16) tmem_st16(R_H + lane_off + h * 64 + c16 * 16, r);
                     }
                     tmem_st_wait();
                 } else {
@@ -953,14 +953,14 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     if (kPre && t == 0 && (!kWide || h == 0)) a.logdec[2 * ticket + hs] = ldsum;
                 }
 #pragma unroll 1
-                for (int c4 = 0; c4 < kP / 4; ++c4) {
-                    uint32_t r[4];
-                    tmem_ld4(R_H + lane_off + h * 64 + c4 * 4, r);
+                for (int c16 = 0; c16 < kP / 16; ++c16) {
+                    uint32_t r[16];
+                    tmem_ld16(R_H + lane_off + h * 64 + c16 * 16, r);
                     tmem_ld_wait();
                     if (dst) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            __stcg(dst + (c4 * 4 + q) * NS + n_row, __uint_as_float(r[q]));
+                        for (int q = 0; q < 16; ++q)
+                            __stcg(dst + (c16 * 16 + q) * NS + n_row, __uint_as_float(r[q]));
                     }
                 }
                 tc_fence_before();
@@ -1107,12 +1107,13 @@ int sm_count() {
     return n > 0 ? n : 148;
 }
 
-// Fewest blocks per CTA for which splitting lanes between CTAs pays.  The
-// state-only pre run costs about 0.7 of a full run per block (its per-block
-// latency chain stays), so a split with B blocks per CTA takes ~1.7 B block
-// times against a whole lane's; with 8 per CTA the small b2 x 12-pair layer
-// (16 blocks per lane) measured 82 us split against 72 us whole.
-constexpr int64_t kChainMinBlocks = 16;
+// When splitting lanes between CTAs pays.  A split call runs three kernels,
+// which costs a fixed ~15 us, and the state-only pre run adds about a third
+// of a block's time per block.  Measured on 24 lanes of 16 blocks: 4 blocks
+// per CTA 56 us against 70 us whole; on 24 lanes of 8 blocks every split was
+// slower than the whole lanes.
+constexpr int64_t kChainMinLaneBlocks = 16;   // blocks per lane
+constexpr int64_t kChainMinCtaBlocks = 4;     // blocks per CTA
 
 struct FLayout {
     size_t hdr, slots, logdec, hstart, seqblk, total;
@@ -1140,13 +1141,10 @@ FLayout fused_layout(const Problem &p) {
     int64_t grid;
     if (p.cu) {
         grid = min64(sms, ptot * nb);
-    } else if ((int64_t)p.nseq * ptot * 2 <= min64(sms, (int64_t)p.nseq * ptot * nb / kChainMinBlocks)) {
-        // At most half as many lanes as CTAs could take at kChainMinBlocks
-        // blocks each: lanes are split between CTAs, which start from the
-        // pre run's records.  Below that many blocks per CTA the second run
-        // and the per-split start and end cost more than the parallelism
-        // gains.
-        grid = min64(sms, (int64_t)p.nseq * ptot * nb / kChainMinBlocks);
+    } else if ((int64_t)p.nseq * ptot * 2 <= sms && nb >= kChainMinLaneBlocks) {
+        // At most half as many lanes as SMs, and long enough: lanes are split
+        // between CTAs, which start from the pre run's records.
+        grid = min64(sms, (int64_t)p.nseq * ptot * nb / kChainMinCtaBlocks);
         w.chain = true;
     } else {
         grid = min64(sms, (int64_t)p.nseq * ptot);

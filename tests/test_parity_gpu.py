@@ -300,10 +300,11 @@ def test_wide_lanes_packed_sequences(segs):
 # second run produces y.
 
 @pytest.mark.parametrize("wi,kw", [
-    (1, dict(seed=61, batch=1, seqlen=8192, nheads=24, init_states=True)),   # 12 lanes, 4 CTAs each
-    (1, dict(seed=62, batch=1, seqlen=6000, nheads=6, init_states=True)),    # ranges straddle lanes
+    (1, dict(seed=61, batch=1, seqlen=8192, nheads=24, init_states=True)),   # 12 lanes on all SMs, ranges straddle
+    (1, dict(seed=62, batch=1, seqlen=6000, nheads=6, init_states=True)),    # 3 lanes, ragged tail
     (3, dict(seed=63, batch=1, seqlen=8192, nheads=8, init_states=True)),    # wide lanes
-], ids=["narrow", "straddle", "wide"])
+    (1, dict(seed=64, batch=2, seqlen=2048, nheads=24, init_states=True)),   # 4 blocks per CTA, lane-aligned
+], ids=["narrow", "straddle", "wide", "four_blocks"])
 def test_split_lanes_two_runs(wi, kw):
     inp = ssd_synth.make_inputs(W[wi], **kw)
     _compare_full(inp, "tc")
