@@ -126,6 +126,9 @@ SCAN_CASES = [
                    segment_lengths=[300, 1, 450, 0, 249])),
     (4, "simt", dict(seed=10, seqlen=600, nheads=4, segment_lengths=[100, 380, 120])),
     (3, "tc2", dict(seed=11, batch=1, seqlen=512, nheads=8)),
+    # few long lanes: split between CTAs (state-only pre run, fold, main run)
+    (1, "tc", dict(seed=13, batch=1, seqlen=4096, nheads=8, init_states=True)),
+    (3, "tc", dict(seed=14, batch=1, seqlen=4096, nheads=8, init_states=True)),
 ]
 
 
