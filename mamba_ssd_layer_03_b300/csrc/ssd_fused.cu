@@ -17,7 +17,12 @@
 // split between two CTAs, the earlier CTA hands the state at the split point
 // to the later one through global memory; every CTA processes the lane it
 // hands off first and the lane it receives last, so the receiver rarely
-// waits.
+// waits.  With few long lanes (at most half as many as SMs) every lane is
+// split several ways, and waiting would chain the CTAs of a lane.  Such a
+// call runs the kernel twice: a state-only first run records each CTA's
+// partial state and decay where its range splits a lane,
+// k_fused_chain_fold passes the state across the splits, and the second
+// run starts every split from its folded state.
 //
 // Per block (tokens i, j in [0, 128), heads h of the lane, state H_h[p][n]
 // at the block start, cs_h = within-block cumulative sum of dt*A_h):
