@@ -18,6 +18,17 @@ Two independent formulations, both in fp64:
   sum is formed directly as a sum over its own range, never as a difference
   of two cumulative sums.
 
+A third formulation, the algorithm the pages give for evaluating that matrix
+product (QbitAI article, section "Mamba-2：更强学习能力，更快训练推理": block
+decomposition of the semiseparable matrix into chunk-local masked quadratic
+products plus a recurrence between chunks):
+
+* ``chunked`` -- per chunk of ``chunk`` tokens, in the pages' order: the
+  cumulative decay within the chunk (``chunk_decay``), the chunk's state
+  contribution (``chunk_state``), the state passed from chunk to chunk
+  (``state_passing``), and the chunk's output from its masked block and its
+  entry state (``chunk_output``).  Chunks restart at every sequence start.
+
 Two helpers around them, also fp64:
 
 * ``dt_transform`` -- the step size Delta = tau_Delta(parameter + s_Delta(x))
@@ -34,7 +45,8 @@ formulations because both are written from the same definition.
 
 Parity unpinned: nothing.  Every function here is pinned by the tests in
 ``tests/test_oracle_pins.py`` against closed forms, hand-computed golden
-fixtures, the recurrent/quadratic duality, and invariants.
+fixtures, the recurrent/quadratic duality, the chunked form's agreement with
+both at every chunk size, and invariants.
 """
 from __future__ import annotations
 
@@ -234,4 +246,78 @@ def quadratic(x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None):
             for j in range(T):
                 F = F + np.exp(np.sum(a[j + 1:])) * dts[j] * np.outer(Xs[j], Bs[j])
             fin[s, h] = F
+    return y, fin
+
+
+# ---------------------------------------------------------------- block decomposition
+# QbitAI article "新架构Mamba更新二代！", section "Mamba-2：更强学习能力，更快训练推理":
+# the semiseparable matrix is cut into chunks; diagonal blocks are masked
+# quadratic products, off-diagonal blocks are low rank and pass through a
+# per-chunk state.  Notation per (sequence, head): a_k = dt_k A_h, tokens of
+# one chunk indexed i, j from 0.
+
+
+def chunk_decay(a: np.ndarray) -> np.ndarray:
+    """Cumulative decay within one chunk: cs_i = a_0 + ... + a_i."""
+    return np.cumsum(a)
+
+
+def chunk_state(Bc: np.ndarray, Xc: np.ndarray, dtc: np.ndarray, cs: np.ndarray) -> np.ndarray:
+    """State the chunk's own tokens leave at its end, from a zero entry state:
+    S = sum_j exp(cs_last - cs_j) dt_j x_j (outer) B_j, shape (P, N)."""
+    w = np.exp(cs[-1] - cs) * dtc                       # (T,)
+    return (Xc * w[:, None]).T @ Bc
+
+
+def state_passing(S: Sequence[np.ndarray], cs_last: Sequence[float], S0: np.ndarray):
+    """Entry state of every chunk and the final state:
+    H_0 = S0, H_{c+1} = exp(cs_last_c) H_c + S_c."""
+    entries = []
+    Hc = S0
+    for Sc, e in zip(S, cs_last):
+        entries.append(Hc)
+        Hc = np.exp(e) * Hc + Sc
+    return entries, Hc
+
+
+def chunk_output(Cc, Bc, Xc, dtc, cs, H_entry, Dh) -> np.ndarray:
+    """Output of one chunk: y_i = sum_{j<=i} (C_i . B_j) exp(cs_i - cs_j) dt_j x_j
+    + exp(cs_i) C_i . H_entry + D_h x_i, shape (T, P)."""
+    T = len(cs)
+    causal = np.tril(np.ones((T, T), dtype=bool))       # j <= i
+    Lmask = np.where(causal, np.exp(np.where(causal, cs[:, None] - cs[None, :], 0.0)), 0.0) * dtc[None, :]
+    y = ((Cc @ Bc.T) * Lmask) @ Xc
+    y += np.exp(cs)[:, None] * (Cc @ H_entry.T)
+    if Dh is not None:
+        y += Dh * Xc
+    return y
+
+
+def chunked(x, dt, A, B, C, D=None, initial_states=None, cu_seqlens=None, chunk: int = 64):
+    """fp64 block decomposition with chunks of ``chunk`` tokens (the last chunk
+    of a sequence may be shorter).  Returns (y, final_states) as float64."""
+    if chunk < 1:
+        raise ValueError("chunk must be positive")
+    x, dt, A, B, C, D, init, cu, (b, L, H, P, N, G, nseq) = _prep(
+        x, dt, A, B, C, D, initial_states, cu_seqlens)
+    y = np.zeros((b, L, H, P))
+    fin = np.zeros((nseq, H, P, N))
+    hpg = H // G
+    for s in range(nseq):
+        row = 0 if cu is not None else s
+        t0 = int(cu[s]) if cu is not None else 0
+        t1 = int(cu[s + 1]) if cu is not None else L
+        for h in range(H):
+            g = h // hpg
+            S0 = init[s, h] if init is not None else np.zeros((P, N))
+            bounds = [(c, min(c + chunk, t1)) for c in range(t0, t1, chunk)]
+            parts = []
+            for c0, c1 in bounds:
+                dtc = dt[row, c0:c1, h]
+                cs = chunk_decay(dtc * A[h])
+                parts.append((dtc, cs, chunk_state(B[row, c0:c1, g], x[row, c0:c1, h], dtc, cs)))
+            entries, fin[s, h] = state_passing([p[2] for p in parts], [p[1][-1] for p in parts], S0)
+            for (c0, c1), (dtc, cs, _), He in zip(bounds, parts, entries):
+                y[row, c0:c1, h] = chunk_output(C[row, c0:c1, g], B[row, c0:c1, g], x[row, c0:c1, h],
+                                                dtc, cs, He, None if D is None else D[h])
     return y, fin

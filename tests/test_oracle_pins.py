@@ -10,7 +10,10 @@
   in (x, initial_states); the unit subset equals the full run;
 * a one-sided check that a huge dt with A < 0 replaces the state by the
   current input (boundary resetting, Mamba-1 walkthrough section 三 2.3);
-* planted mistakes in the oracle are caught by at least one of these pins.
+* planted mistakes in the oracle are caught by at least one of these pins;
+* the block decomposition (chunked form) agrees with both formulations at
+  every chunk size, its steps meet their closed forms, and a mistake planted
+  in any one step breaks that agreement.
 """
 import glob
 import json
@@ -45,8 +48,17 @@ def _golden_cases():
     return sorted(glob.glob(os.path.join(GOLDEN, "*.json")))
 
 
+FORMS = {
+    "recurrent": oracle.recurrent,
+    "quadratic": oracle.quadratic,
+    "chunked1": lambda **kw: oracle.chunked(chunk=1, **kw),
+    "chunked2": lambda **kw: oracle.chunked(chunk=2, **kw),
+    "chunked64": lambda **kw: oracle.chunked(chunk=64, **kw),
+}
+
+
 @pytest.mark.parametrize("path", _golden_cases(), ids=lambda p: os.path.basename(p))
-@pytest.mark.parametrize("form", ["recurrent", "quadratic"])
+@pytest.mark.parametrize("form", sorted(FORMS))
 def test_golden_fixture(path, form):
     with open(path) as f:
         g = json.load(f)
@@ -55,7 +67,7 @@ def test_golden_fixture(path, form):
                 C=np.array(g["C"]), D=np.array(g["D"]),
                 initial_states=None if g["initial_states"] is None else np.array(g["initial_states"]),
                 cu_seqlens=g["cu_seqlens"])
-    y, fin = getattr(oracle, form)(**args)
+    y, fin = FORMS[form](**args)
     np.testing.assert_allclose(y, np.array(g["y"]), rtol=0, atol=1e-12)
     np.testing.assert_allclose(fin, np.array(g["final_states"]), rtol=0, atol=1e-12)
 
@@ -312,3 +324,105 @@ def test_step_closed_form():
         Sp = math.exp(d * float(A[h])) * S0[0, h].numpy() + d * np.outer(x[0, 0, h].numpy(), B[0, 0, 0].numpy())
         np.testing.assert_allclose(S[0, h], Sp, rtol=1e-13)
         np.testing.assert_allclose(y[0, h], Sp @ C[0, 0, 0].numpy() + float(D[h]) * x[0, 0, h].numpy(), rtol=1e-13)
+
+
+# ---------------------------------------------------------------- block decomposition
+
+def _rel(a, b):
+    return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-300))
+
+
+@pytest.mark.parametrize("chunk", [1, 2, 3, 7, 16, 40, 64])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_chunked_equals_recurrent(chunk, seed):
+    case = _rand_case(seed, b=2, L=40, H=4, P=3, N=5, G=2)
+    yr, fr = oracle.recurrent(**case)
+    yc, fc = oracle.chunked(chunk=chunk, **case)
+    assert _rel(yc, yr) < 1e-12 and _rel(fc, fr) < 1e-12
+
+
+@pytest.mark.parametrize("chunk", [1, 3, 8])
+def test_chunked_equals_quadratic_packed(chunk):
+    # packed sequences, one of them empty and one a single token: chunks restart
+    # at every sequence start
+    case = _rand_case(5, b=1, L=23, H=2, P=2, N=3, G=1, cu=[0, 9, 9, 10, 23])
+    yq, fq = oracle.quadratic(**case)
+    yc, fc = oracle.chunked(chunk=chunk, **case)
+    assert _rel(yc, yq) < 1e-12 and _rel(fc, fq) < 1e-12
+
+
+def test_chunk_state_closed_forms():
+    rng = np.random.default_rng(3)
+    X, Bm = rng.standard_normal((1, 4)), rng.standard_normal((1, 6))
+    dtv = np.array([0.3])
+    # one token: its own contribution dt x (outer) B, undecayed
+    S = oracle.chunk_state(Bm, X, dtv, oracle.chunk_decay(dtv * -2.0))
+    np.testing.assert_allclose(S, 0.3 * np.outer(X[0], Bm[0]), rtol=1e-15)
+    # A = 0: no decay, the plain sum of dt_j x_j (outer) B_j
+    X, Bm, dtv = rng.standard_normal((5, 4)), rng.standard_normal((5, 6)), rng.uniform(0.1, 1, 5)
+    S = oracle.chunk_state(Bm, X, dtv, oracle.chunk_decay(np.zeros(5)))
+    np.testing.assert_allclose(S, sum(dtv[j] * np.outer(X[j], Bm[j]) for j in range(5)), rtol=1e-13)
+    # first token of two, decay a_1 = ln(1/2) applied to it once
+    X, Bm, dtv = np.ones((2, 1)), np.ones((2, 1)), np.ones(2)
+    S = oracle.chunk_state(Bm, X, dtv, oracle.chunk_decay(np.array([math.log(0.25), math.log(0.5)])))
+    np.testing.assert_allclose(S, [[0.5 + 1.0]], rtol=1e-15)
+
+
+def test_state_passing_closed_forms():
+    S0 = np.full((2, 2), 3.0)
+    zeros = [np.zeros((2, 2))] * 3
+    entries, final = oracle.state_passing(zeros, [math.log(0.5)] * 3, S0)
+    # no input: the entry states halve from chunk to chunk
+    for c, e in enumerate(entries):
+        np.testing.assert_allclose(e, S0 * 0.5 ** c, rtol=1e-15)
+    np.testing.assert_allclose(final, S0 / 8, rtol=1e-15)
+    # no decay: the entry states are prefix sums of the chunk states
+    S = [np.full((2, 2), float(c + 1)) for c in range(3)]
+    entries, final = oracle.state_passing(S, [0.0] * 3, np.zeros((2, 2)))
+    np.testing.assert_allclose(entries[2], np.full((2, 2), 3.0))
+    np.testing.assert_allclose(final, np.full((2, 2), 6.0))
+
+
+def test_chunk_output_closed_forms():
+    rng = np.random.default_rng(4)
+    Cc, Bc, Xc = rng.standard_normal((1, 5)), rng.standard_normal((1, 5)), rng.standard_normal((1, 3))
+    # one token, zero entry state: (C . B) dt x + D x
+    y = oracle.chunk_output(Cc, Bc, Xc, np.array([0.2]), np.array([-0.7]), np.zeros((3, 5)), 1.5)
+    np.testing.assert_allclose(y, (Cc[0] @ Bc[0]) * 0.2 * Xc + 1.5 * Xc, rtol=1e-14)
+    # dt = 0 everywhere: only the entry state, undecayed, read through C
+    H = rng.standard_normal((3, 5))
+    Cc, Bc, Xc = rng.standard_normal((4, 5)), rng.standard_normal((4, 5)), rng.standard_normal((4, 3))
+    y = oracle.chunk_output(Cc, Bc, Xc, np.zeros(4), np.zeros(4), H, None)
+    np.testing.assert_allclose(y, Cc @ H.T, rtol=1e-14)
+
+
+def _planted(monkeypatch, step, fn):
+    monkeypatch.setattr(oracle, step, fn)
+
+
+PLANTED = {
+    # the entry state's decay forgotten between chunks
+    "no_decay_between_chunks": ("state_passing", lambda S, e, S0: _STATE_PASSING(S, [0.0] * len(e), S0)),
+    # the chunk state weighted by the decay from the chunk start instead of to its end
+    "state_weight_reversed": ("chunk_state", lambda Bc, Xc, dtc, cs: ((Xc * (np.exp(cs - cs[0]) * dtc)[:, None]).T @ Bc)),
+    # the mask's diagonal dropped (j < i instead of j <= i)
+    "strict_mask": ("chunk_output", lambda Cc, Bc, Xc, dtc, cs, He, Dh: _CHUNK_OUTPUT(Cc, Bc, Xc, dtc, cs, He, Dh)
+                    - ((Cc * Bc).sum(1) * dtc)[:, None] * Xc),
+    # the entry state read without its decay into the chunk
+    "entry_undecayed": ("chunk_output", lambda Cc, Bc, Xc, dtc, cs, He, Dh: _CHUNK_OUTPUT(Cc, Bc, Xc, dtc, cs, He, Dh)
+                        + (1.0 - np.exp(cs))[:, None] * (Cc @ He.T)),
+    # the cumulative decay shifted by one token (exclusive instead of inclusive)
+    "exclusive_cumsum": ("chunk_decay", lambda a: np.concatenate([[0.0], np.cumsum(a)[:-1]])),
+}
+_CHUNK_OUTPUT = oracle.chunk_output
+_STATE_PASSING = oracle.state_passing
+
+
+@pytest.mark.parametrize("name", sorted(PLANTED))
+def test_chunked_planted_mistakes_are_caught(name, monkeypatch):
+    step, fn = PLANTED[name]
+    case = _rand_case(7, b=1, L=24, H=2, P=3, N=4, G=1)
+    yr, fr = oracle.recurrent(**case)
+    _planted(monkeypatch, step, fn)
+    yc, fc = oracle.chunked(chunk=8, **case)
+    assert max(_rel(yc, yr), _rel(fc, fr)) > 1e-3
