@@ -29,6 +29,11 @@
  *   applies no softplus, bias or clamp.  The chunk size changes only the
  *   rounding, never the result.
  *
+ * Value domain.  As in the method, every decay exp(dt_t * A_h) lies in
+ * (0, 1]: dt >= 0 and A_h <= 0.  The kernels rely on it (their exponents are
+ * never positive).  These values live in device memory and are not checked;
+ * outside this domain the results are unspecified.
+ *
  * Layouts.  Row-major, contiguous, no padding:
  *   x, y            [batch][seqlen][nheads][headdim]   dtype (fp32 or bf16)
  *   dt              [batch][seqlen][nheads]            fp32
@@ -107,7 +112,8 @@ typedef enum ssd_status {
 
 typedef struct ssd_shape {
     int64_t batch;       /* >= 0 */
-    int64_t seqlen;      /* >= 0, tokens per batch row */
+    int64_t seqlen;      /* >= 0, tokens per batch row (at most 2^31 - 1; every
+                            buffer at most 2^56 elements) */
     int32_t nheads;      /* H >= 1 */
     int32_t headdim;     /* P, 1..256 (SIMT); 64 (TC) */
     int32_t dstate;      /* N, 1..256 (SIMT); 64, 128 or 256 (TC) */

@@ -74,6 +74,12 @@ def test_workspace_size_simt_scales_with_chunks():
     (dict(headdim=300, algo="simt"), 2),
     (dict(dstate=512, algo="simt"), 2),
     (dict(seqlen=-1), 1),
+    (dict(seqlen=2**31), 2),
+    # buffers that could not exist: rejected before any size is computed from them
+    (dict(batch=2**40, seqlen=2**30), 2),
+    (dict(batch=2**33, seqlen=2**24, nseq=2**33), 2),
+    (dict(batch=1, seqlen=2**24, nheads=2**30, ngroups=1, algo="simt"), 2),          # x: 2^60 elements
+    (dict(batch=2**20, seqlen=1, nseq=2**31 - 1, nheads=2**12, dstate=256, algo="simt"), 2),  # states: 2^57
 ])
 def test_workspace_size_rejects(kw, code):
     with pytest.raises(ssd.SsdError) as ei:
