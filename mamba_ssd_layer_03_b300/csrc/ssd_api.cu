@@ -18,23 +18,13 @@ __global__ void validate_cu_kernel(const int32_t *cu, int nseq, int64_t seqlen, 
     if (bad) set_status(status, SSD_ERR_DEVICE_INPUT);
 }
 
-// Element counts of x/y, B/C and the states, in 128-bit arithmetic: a shape
-// whose buffers could not exist is rejected before any size computed from it
-// can wrap around.
-bool too_large(const ssd_shape *s) {
-    const __int128 tokens = (__int128)s->batch * s->seqlen;
-    const __int128 lim = (__int128)1 << 56;
-    return tokens * s->nheads * s->headdim > lim || tokens * s->ngroups * s->dstate > lim ||
-           (__int128)s->nseq * s->nheads * s->headdim * s->dstate > lim;
-}
-
 // Host-side checks that need no device access.  Fills `p` on success.
 int resolve(const ssd_shape *s, Problem &p, int *algo_out) {
     if (!s) return SSD_ERR_INVALID_ARG;
     if (s->batch < 0 || s->seqlen < 0 || s->nheads < 1 || s->headdim < 1 || s->dstate < 1 ||
         s->ngroups < 1 || s->nheads % s->ngroups != 0 || s->nseq < 0)
         return SSD_ERR_INVALID_ARG;
-    if (s->seqlen > (int64_t)INT32_MAX || too_large(s)) return SSD_ERR_UNSUPPORTED;
+    if (s->seqlen > (int64_t)INT32_MAX || shape_too_large(s)) return SSD_ERR_UNSUPPORTED;
     if (s->dtype != SSD_F32 && s->dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
     if (s->chunk_size != 64 && s->chunk_size != 128 && s->chunk_size != 256)
         return SSD_ERR_UNSUPPORTED;

@@ -72,4 +72,14 @@ cudaError_t launch_validate_cu(const Problem &p);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Element counts of x/y, B/C and the states of a scan shape, in 128-bit
+// arithmetic: a shape whose buffers could not exist (over 2^56 elements) is
+// rejected before any size computed from it can wrap around.
+inline bool shape_too_large(const ssd_shape *s) {
+    const __int128 tokens = (__int128)s->batch * s->seqlen;
+    const __int128 lim = (__int128)1 << 56;
+    return tokens * s->nheads * s->headdim > lim || tokens * s->ngroups * s->dstate > lim ||
+           (__int128)s->nseq * s->nheads * s->headdim * s->dstate > lim;
+}
+
 }  // namespace ssd

@@ -71,7 +71,7 @@ extern "C" SSD_API int ssd_scan_noalloc(const ssd_shape *s, const void *x, const
     if (s->batch < 1 || s->seqlen < 1 || s->nheads < 1 || s->headdim < 1 || s->dstate < 1 ||
         s->ngroups < 1 || s->nheads % s->ngroups != 0 || s->nseq != s->batch)
         return SSD_ERR_INVALID_ARG;
-    if (s->seqlen > (int64_t)INT32_MAX) return SSD_ERR_UNSUPPORTED;
+    if (s->seqlen > (int64_t)INT32_MAX || shape_too_large(s)) return SSD_ERR_UNSUPPORTED;
     if (s->algo != SSD_ALGO_AUTO && s->algo != SSD_ALGO_TC) return SSD_ERR_UNSUPPORTED;
     if (!x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
 

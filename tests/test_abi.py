@@ -208,3 +208,14 @@ def test_selftest_rejects_bad_arguments():
     fake = ctypes.c_void_p(1 << 20)
     assert lib.ssd_selftest_wait_timeout(2, fake, None) == 1
     assert lib.ssd_selftest_wait_timeout(0, None, None) == 1
+
+
+def test_noalloc_rejects_oversized_shape_on_host():
+    # checked before the scratch, the device or any pointer is touched
+    import ctypes
+    lib = ssd.load_library()
+    shape = _shape(batch=1, seqlen=2**24, nheads=2**30, ngroups=1, nseq=1, algo="tc")
+    fake = ctypes.c_void_p(1 << 20)
+    rc = lib.ssd_scan_noalloc(ctypes.byref(shape), fake, fake, fake, fake, fake, None, None, fake,
+                              None, None, None)
+    assert rc == 2, ssd.status_string(rc)
