@@ -218,11 +218,19 @@ def ssd_scan(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor
     tf = make_dt_transform(dt_bias, dt_softplus, dt_limit)
     shape = make_shape(b, L, H, P, N, G, chunk_size, nseq, x.dtype, algo)
     nbytes = workspace_size(shape, tf)
+    # caller-supplied buffers are checked like the inputs: the kernels write
+    # exactly the documented extents
+    if workspace is not None:
+        _check(workspace, "workspace", torch.uint8, device=dev)
     if workspace is None or workspace.numel() < nbytes:
         workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    if out is not None:
+        _check(out, "out", x.dtype, tuple(x.shape), dev)
     y = out if out is not None else torch.empty_like(x)
     fin = None
     if return_final_states:
+        if final_out is not None:
+            _check(final_out, "final_out", torch.float32, (nseq, H, P, N), dev)
         fin = final_out if final_out is not None else torch.empty(
             (nseq, H, P, N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev).cuda_stream
@@ -255,6 +263,10 @@ def ssd_scan_noalloc(x, dt, A, B, C, D=None, chunk_size=256, initial_states=None
     b, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     shape = make_shape(b, L, H, P, N, G, chunk_size, b, x.dtype, "tc")
+    if out is not None:
+        _check(out, "out", x.dtype, tuple(x.shape), x.device)
+    if final_out is not None:
+        _check(final_out, "final_out", torch.float32, (b, H, P, N), x.device)
     y = out if out is not None else torch.empty_like(x)
     stream = torch.cuda.current_stream(x.device).cuda_stream
     rc = lib.ssd_scan_noalloc(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
@@ -297,6 +309,8 @@ def ssd_step(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor
         raise TypeError(f"x/B/C dtype must be float32 or bfloat16, got {x.dtype}")
     shape = SsdStepShape(b, H, P, N, G, dtype, 0)
     tf = make_dt_transform(dt_bias, dt_softplus, dt_limit)
+    if out is not None:
+        _check(out, "out", x.dtype, (b, H, P), dev)
     y = out if out is not None else torch.empty_like(x)
     stream = torch.cuda.current_stream(dev).cuda_stream
     rc = lib.ssd_step(ctypes.byref(shape), _ptr(x), _ptr(dt),

@@ -219,3 +219,30 @@ def test_noalloc_rejects_oversized_shape_on_host():
     rc = lib.ssd_scan_noalloc(ctypes.byref(shape), fake, fake, fake, fake, fake, None, None, fake,
                               None, None, None)
     assert rc == 2, ssd.status_string(rc)
+
+
+@pytest.mark.parametrize("bad", ["out_shape", "out_dtype", "final_shape", "workspace_dtype"])
+def test_scan_checks_caller_buffers_before_any_device_work(bad):
+    # meta tensors pass the input checks; a wrong caller-supplied buffer must be
+    # refused before the library, the stream or any memory is touched
+    import torch
+    m = dict(device="meta")
+    b, L, H, P, N = 2, 300, 4, 64, 128
+    x = torch.empty(b, L, H, P, dtype=torch.bfloat16, **m)
+    dt = torch.empty(b, L, H, **m)
+    A = torch.empty(H, **m)
+    B = torch.empty(b, L, 1, N, dtype=torch.bfloat16, **m)
+    kw = dict(out=torch.empty(b, L, H, P, dtype=torch.bfloat16, **m),
+              final_out=torch.empty(b, H, P, N, **m))
+    if bad == "out_shape":
+        kw["out"] = torch.empty(b, L, H, P + 1, dtype=torch.bfloat16, **m)
+    elif bad == "out_dtype":
+        kw["out"] = torch.empty(b, L, H, P, **m)
+    elif bad == "final_shape":
+        kw["final_out"] = torch.empty(b, H, P, N // 2, **m)
+    else:
+        kw["workspace"] = torch.empty(1 << 20, dtype=torch.float32, **m)
+    expect = {"out_shape": "out has shape", "out_dtype": "out must be", "final_shape": "final_out has shape",
+              "workspace_dtype": "workspace must be"}[bad]
+    with pytest.raises((ValueError, TypeError), match=expect):
+        ssd.ssd_scan(x, dt, A, B, B, None, 256, algo="simt", **kw)
