@@ -2,7 +2,7 @@
 roofline, next to the fp64 CPU oracle.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 2] [--algo auto|simt|tc]
+                    [--workload 2] [--algo auto|simt|tc|tc2]
 
 A step is one ssd_scan() over the whole workload (default: the 2.7B-shaped
 SSD layer, batch 4 x 8192 tokens, 80 heads, P=64, N=128, chunk 256, bf16),
@@ -244,7 +244,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=2)
-    ap.add_argument("--algo", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--algo", default="auto", choices=["auto", "simt", "tc", "tc2"])
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
