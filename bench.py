@@ -248,6 +248,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=None,
+                    help="seconds of oracle work per step of --impl reference (default: the "
+                         "run's 150 s spread over its steps, 1 to 20 s each)")
     ap.add_argument("--seqlen", type=int, default=None,
                     help="override the workload's tokens per sequence (profiling captures)")
     ap.add_argument("--op", default="scan", choices=["scan", "step"])
@@ -625,7 +628,8 @@ def run_reference(args, w, rank, world):
         return
     import oracle
     inp = ssd_synth.make_inputs(w, seed=0)
-    budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    budget = args.ref_budget if args.ref_budget else max(
+        1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         time_oracle_sample(inp, budget)
     rates, secs_total, units_total = [], 0.0, 0
@@ -636,7 +640,7 @@ def run_reference(args, w, rank, world):
         units_total += units
     value = statistics.mean(rates)
     tokens = inp["batch"] * inp["seqlen"]
-    sample = (f"each step: about {budget:.0f} s of (sequence, head) units of the same workload "
+    sample = (f"each step: about {budget:.3g} s of (sequence, head) units of the same workload "
               f"(full length, fp64 recurrence); tokens/s = unit-tokens / nheads / seconds")
     out = {
         "impl": "reference", "metric": "SSD fwd tokens/s (TFLOP/s and % of roofline alongside) on 1 B300",
