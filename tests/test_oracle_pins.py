@@ -426,3 +426,80 @@ def test_chunked_planted_mistakes_are_caught(name, monkeypatch):
     _planted(monkeypatch, step, fn)
     yc, fc = oracle.chunked(chunk=8, **case)
     assert max(_rel(yc, yr), _rel(fc, fr)) > 1e-3
+
+
+# ---------------------------------------------------------------- one unit
+# oracle.recurrent_unit checks the full-size workloads one (sequence, head) at
+# a time and is the CPU baseline's timed code.  It slices the inputs down to
+# one unit (the head's group, the sequence's row or packed range, its initial
+# state) and runs the recurrence on them; the recurrence itself is pinned
+# above, so what is pinned here is the slicing: every unit must equal, bit for
+# bit, the same unit of one run over all the inputs.
+
+def _unit_cases():
+    return {
+        # G > 1: heads 0-2 use group 0, heads 3-5 group 1, heads 6-8 group 2
+        "groups": _rand_case(81, b=2, L=37, H=9, P=3, N=4, G=3),
+        # packed sequences with initial states, an empty sequence in the middle
+        "packed": _rand_case(82, b=1, L=50, H=4, P=2, N=3, G=2, cu=[0, 13, 13, 41, 50]),
+        # no D, no initial states, one group per head
+        "bare": _rand_case(83, b=3, L=20, H=2, P=3, N=2, G=2, init=False, D=False),
+    }
+
+
+def _unit_mismatches(unit_fn, c):
+    """(s, h) units where unit_fn's result differs from the full run's."""
+    y, fin = oracle.recurrent(**c)
+    cu = c["cu_seqlens"]
+    nseq = fin.shape[0]
+    bad = []
+    for s in range(nseq):
+        for h in range(c["x"].shape[2]):
+            yu, fu = unit_fn(c["x"], c["dt"], c["A"], c["B"], c["C"], c["D"],
+                             c["initial_states"], cu, s, h)
+            row, t0, t1 = (0, int(cu[s]), int(cu[s + 1])) if cu is not None else (s, 0, y.shape[1])
+            if yu.shape != (t1 - t0, y.shape[3]) or not (
+                    np.array_equal(yu, y[row, t0:t1, h]) and np.array_equal(fu, fin[s, h])):
+                bad.append((s, h))
+    return bad
+
+
+@pytest.mark.parametrize("case", sorted(_unit_cases()))
+def test_recurrent_unit_equals_slice_of_full_run(case):
+    c = _unit_cases()[case]
+    assert _unit_mismatches(oracle.recurrent_unit, c) == []
+
+
+def test_recurrent_unit_empty_sequence_keeps_initial_state():
+    c = _unit_cases()["packed"]
+    yu, fu = oracle.recurrent_unit(c["x"], c["dt"], c["A"], c["B"], c["C"], c["D"],
+                                   c["initial_states"], c["cu_seqlens"], 1, 2)
+    assert yu.shape == (0, 2)
+    np.testing.assert_array_equal(fu, c["initial_states"][1, 2].numpy())
+
+
+def _unit_wrong_group(x, dt, A, B, C, D, S0, cu, s, h):
+    # plausible slip: group h % G instead of h // (H / G)
+    G = B.shape[2]
+    sl = (lambda t, k: t[s:s + 1, :, k:k + 1]) if cu is None else \
+        (lambda t, k: t[0:1, int(cu[s]):int(cu[s + 1]), k:k + 1])
+    dts = dt[s:s + 1, :, h:h + 1] if cu is None else dt[0:1, int(cu[s]):int(cu[s + 1]), h:h + 1]
+    y, fin = oracle.recurrent(sl(x, h), dts, A[h:h + 1], sl(B, h % G), sl(C, h % G),
+                              None if D is None else D[h:h + 1],
+                              None if S0 is None else S0[s:s + 1, h:h + 1], None)
+    return y[0, :, 0, :], fin[0, 0]
+
+
+def _unit_wrong_state_row(x, dt, A, B, C, D, S0, cu, s, h):
+    # plausible slip: the initial state of sequence s taken from the batch row
+    # (row 0 for every packed sequence)
+    row = s if cu is None else 0
+    S0r = None if S0 is None else S0[row:row + 1]
+    return oracle.recurrent_unit(x, dt, A, B, C, D, S0r if S0 is None else
+                                 S0r.expand(S0.shape[0], *S0.shape[1:]), cu, s, h)
+
+
+def test_recurrent_unit_pin_catches_slicing_mistakes():
+    cases = _unit_cases()
+    assert _unit_mismatches(_unit_wrong_group, cases["groups"]) != []
+    assert _unit_mismatches(_unit_wrong_state_row, cases["packed"]) != []
