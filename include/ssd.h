@@ -273,11 +273,14 @@ SSD_API int ssd_resolve_algo(const ssd_shape *shape);
  *   device_status  nullable DEVICE pointer to one int; if given, the call's
  *                  device status word (SSD_OK or SSD_ERR_DEVICE_TIMEOUT) is
  *                  copied there on `stream` when the scan's work is done.
+ * shape->algo may be SSD_ALGO_AUTO, SSD_ALGO_TC or SSD_ALGO_TC_TWOPASS (all
+ * three run the two-pass kernels); any other value is SSD_ERR_UNSUPPORTED.
  * Returns SSD_ERR_WORKSPACE, before enqueuing anything, if the shape needs
  * more scratch than the 32 MiB array holds (the need is
  * ssd_scan_workspace_size() of the same shape with algo
  * SSD_ALGO_TC_TWOPASS), and SSD_ERR_UNSUPPORTED for shapes the two-pass
- * path does not take.
+ * path does not take (dtype other than bf16, chunk_size other than 128 or
+ * 256, headdim other than 64, dstate other than 128 or 256).
  * Allocates nothing: no cudaMalloc/cudaFree and no allocating library call.
  * All calls share the one array and it keeps the last call's contents (the
  * call clears what must start at zero), so calls whose GPU work overlaps --

@@ -254,24 +254,51 @@ def ssd_scan(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor
 
 
 def ssd_scan_noalloc(x, dt, A, B, C, D=None, chunk_size=256, initial_states=None,
-                     out=None, final_out=None, device_status=None):
+                     out=None, final_out=None, device_status=None, algo: str = "tc"):
     """Scan on the library's own scratch (no workspace, nothing allocated by
     the library).  For callers that cannot allocate device memory while the
     scan runs; outputs may be passed in (``out``, ``final_out``) so that this
-    wrapper allocates nothing either.  Returns (y, final_states or None)."""
+    wrapper allocates nothing either.  ``device_status`` (one int32 on the
+    device, optional) receives the call's device status word.  Inputs are
+    checked like those of ssd_scan(), and the call runs with x's device
+    current (the library picks that device's scratch).  ``algo`` is "tc",
+    "tc2" or "auto": all three run the two-pass tensor-core kernels.
+    Returns (y, final_states or None)."""
     lib = load_library()
+    if not isinstance(x, torch.Tensor) or x.dim() != 4:
+        raise ValueError("x must be a (batch, seqlen, nheads, headdim) tensor")
+    if not isinstance(B, torch.Tensor) or B.dim() != 4:
+        raise ValueError("B must be a (batch, seqlen, ngroups, dstate) tensor")
+    dev = x.device
+    if algo not in ("tc", "tc2", "auto"):
+        raise ValueError("ssd_scan_noalloc runs the two-pass tensor-core kernels: "
+                         "algo must be 'tc', 'tc2' or 'auto'")
     b, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
-    shape = make_shape(b, L, H, P, N, G, chunk_size, b, x.dtype, "tc")
+    _check(x, "x", x.dtype, device=dev)
+    _check(dt, "dt", torch.float32, (b, L, H), dev)
+    _check(A, "A", torch.float32, (H,), dev)
+    _check(B, "B", x.dtype, (b, L, G, N), dev)
+    _check(C, "C", x.dtype, (b, L, G, N), dev)
+    if D is not None:
+        _check(D, "D", torch.float32, (H,), dev)
+    if initial_states is not None:
+        _check(initial_states, "initial_states", torch.float32, (b, H, P, N), dev)
     if out is not None:
-        _check(out, "out", x.dtype, tuple(x.shape), x.device)
+        _check(out, "out", x.dtype, tuple(x.shape), dev)
     if final_out is not None:
-        _check(final_out, "final_out", torch.float32, (b, H, P, N), x.device)
-    y = out if out is not None else torch.empty_like(x)
-    stream = torch.cuda.current_stream(x.device).cuda_stream
-    rc = lib.ssd_scan_noalloc(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
-                              _ptr(D), _ptr(initial_states), _ptr(y), _ptr(final_out),
-                              _ptr(device_status), ctypes.c_void_p(stream))
+        _check(final_out, "final_out", torch.float32, (b, H, P, N), dev)
+    if device_status is not None:
+        _check(device_status, "device_status", torch.int32, (1,), dev)
+    if dev.type != "cuda":
+        raise ValueError("ssd_scan_noalloc runs on CUDA tensors")
+    shape = make_shape(b, L, H, P, N, G, chunk_size, b, x.dtype, algo)
+    with torch.cuda.device(dev):
+        y = out if out is not None else torch.empty_like(x)
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        rc = lib.ssd_scan_noalloc(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(B),
+                                  _ptr(C), _ptr(D), _ptr(initial_states), _ptr(y),
+                                  _ptr(final_out), _ptr(device_status), ctypes.c_void_p(stream))
     if rc != 0:
         raise SsdError(rc, "ssd_scan_noalloc")
     return y, final_out

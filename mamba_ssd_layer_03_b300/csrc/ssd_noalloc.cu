@@ -72,7 +72,12 @@ extern "C" SSD_API int ssd_scan_noalloc(const ssd_shape *s, const void *x, const
         s->ngroups < 1 || s->nheads % s->ngroups != 0 || s->nseq != s->batch)
         return SSD_ERR_INVALID_ARG;
     if (s->seqlen > (int64_t)INT32_MAX || shape_too_large(s)) return SSD_ERR_UNSUPPORTED;
-    if (s->algo != SSD_ALGO_AUTO && s->algo != SSD_ALGO_TC) return SSD_ERR_UNSUPPORTED;
+    if (s->algo != SSD_ALGO_AUTO && s->algo != SSD_ALGO_TC && s->algo != SSD_ALGO_TC_TWOPASS)
+        return SSD_ERR_UNSUPPORTED;
+    // the two-pass kernels' own limits, checked before anything is derived
+    // from the chunk size (a chunk size of 0 must not reach the division below)
+    if (s->dtype != SSD_BF16 || (s->chunk_size != 128 && s->chunk_size != 256))
+        return SSD_ERR_UNSUPPORTED;
     if (!x || !dt || !A || !B || !C || !y) return SSD_ERR_INVALID_ARG;
 
     Problem p;

@@ -246,3 +246,57 @@ def test_scan_checks_caller_buffers_before_any_device_work(bad):
               "workspace_dtype": "workspace must be"}[bad]
     with pytest.raises((ValueError, TypeError), match=expect):
         ssd.ssd_scan(x, dt, A, B, B, None, 256, algo="simt", **kw)
+
+
+@pytest.mark.parametrize("field,value", [("chunk_size", 0), ("chunk_size", 64), ("dtype", 0),
+                                         ("algo", 1)])
+def test_noalloc_rejects_unsupported_shape_before_any_arithmetic(field, value):
+    # a chunk size of 0 must come back as UNSUPPORTED, not divide by zero;
+    # the allocation-free call takes only what the two-pass kernels take
+    import ctypes
+    lib = ssd.load_library()
+    shape = _shape(batch=1, seqlen=300, nheads=2, ngroups=1, nseq=1, algo="tc")
+    setattr(shape, field, value)
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: the shape check comes first
+    rc = lib.ssd_scan_noalloc(ctypes.byref(shape), fake, fake, fake, fake, fake, None, None, fake,
+                              None, None, None)
+    assert rc == 2, ssd.status_string(rc)
+
+
+@pytest.mark.parametrize("bad", ["dt_shape", "A_dtype", "C_shape", "D_shape", "init_shape",
+                                 "x_noncontig", "status_dtype", "algo"])
+def test_noalloc_wrapper_checks_inputs_before_the_library(bad):
+    # meta tensors: every check runs before the library or any memory is touched
+    import torch
+    m = dict(device="meta")
+    b, L, H, P, N = 2, 300, 4, 64, 128
+    a = dict(x=torch.empty(b, L, H, P, dtype=torch.bfloat16, **m), dt=torch.empty(b, L, H, **m),
+             A=torch.empty(H, **m), B=torch.empty(b, L, 1, N, dtype=torch.bfloat16, **m),
+             C=torch.empty(b, L, 1, N, dtype=torch.bfloat16, **m), D=torch.empty(H, **m))
+    kw = {}
+    if bad == "dt_shape":
+        a["dt"] = torch.empty(b, L, H + 1, **m)
+    elif bad == "A_dtype":
+        a["A"] = torch.empty(H, dtype=torch.float64, **m)
+    elif bad == "C_shape":
+        a["C"] = torch.empty(b, L, 1, N // 2, dtype=torch.bfloat16, **m)
+    elif bad == "D_shape":
+        a["D"] = torch.empty(H + 2, **m)
+    elif bad == "init_shape":
+        kw["initial_states"] = torch.empty(b, H, P, N + 1, **m)
+    elif bad == "x_noncontig":
+        a["x"] = torch.empty(b, L, P, H, dtype=torch.bfloat16, **m).transpose(2, 3)
+    elif bad == "status_dtype":
+        kw["device_status"] = torch.empty(1, dtype=torch.int64, **m)
+    else:
+        kw["algo"] = "simt"
+    with pytest.raises((ValueError, TypeError)):
+        ssd.ssd_scan_noalloc(a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], 256, **kw)
+
+
+def test_noalloc_wrapper_refuses_host_tensors():
+    import torch
+    x = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    B = torch.zeros(1, 8, 1, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        ssd.ssd_scan_noalloc(x, torch.zeros(1, 8, 2), torch.zeros(2), B, B, None, 256)
