@@ -308,3 +308,77 @@ def test_wide_lanes_packed_sequences(segs):
 def test_split_lanes_two_runs(wi, kw):
     inp = ssd_synth.make_inputs(W[wi], **kw)
     _compare_full(inp, "tc")
+
+
+# ---------------------------------------------------------------- strong decay
+# Heads whose decay over a few tokens is enormous.  With A = -16 and a constant
+# step dt, 32 tokens decay by exp(-512 dt): about e^-51 at dt = 0.1, e^-77 at
+# dt = 0.15 and e^-512 at dt = 1.  The fused kernel factors the masked block
+# at 32-token sub-blocks and changes method once a sub-block's decay is too
+# large for the factored form, so these cases run both of its methods and the
+# boundary between them; "mixed" gives the two heads of a lane different
+# regimes.  The last case is the limit Delta -> infinity, which replaces the
+# state by the current input (Mamba-1 walkthrough "Mamba: Linear-Time
+# Sequence Modeling with Selective State Spaces", sections 三 2.3 "边界重置"
+# and 三 3).
+
+def _strong_decay(inp, regime, seed):
+    H = inp["nheads"]
+    g = torch.Generator().manual_seed(seed)
+    shape = inp["dt"].shape
+    if regime == "mixed":
+        # per head: 0.02 (weak), 0.1, 0.15, 1.0, cycling, plus noise
+        base = torch.tensor([0.02, 0.1, 0.15, 1.0])[torch.arange(H) % 4]
+        dt = base * (1.0 + 0.2 * torch.rand(shape, generator=g))
+    else:
+        dt = torch.full(shape, float(regime))
+    inp = dict(inp)
+    inp["dt"] = dt.contiguous()
+    inp["A"] = torch.full((H,), -16.0)
+    return inp
+
+
+STRONG = [
+    (1, dict(batch=2, seqlen=700, nheads=6, init_states=True)),     # narrow lanes, one run
+    (3, dict(batch=1, seqlen=520, nheads=8, init_states=True)),     # wide lanes (dstate 256)
+    (1, dict(batch=1, seqlen=4096, nheads=8, init_states=True)),    # narrow, split lanes
+    (3, dict(batch=1, seqlen=4096, nheads=8, init_states=True)),    # wide, split lanes
+]
+
+
+@pytest.mark.parametrize("regime", ["0.1", "0.15", "1.0", "mixed"])
+@pytest.mark.parametrize("wi,kw", STRONG, ids=["narrow", "wide", "narrow_split", "wide_split"])
+def test_strong_decay_fused(wi, kw, regime):
+    inp = _strong_decay(ssd_synth.make_inputs(W[wi], seed=90 + wi, **kw), regime, seed=wi)
+    _compare_full(inp, "tc")
+
+
+@pytest.mark.parametrize("algo", ["simt", "tc2"])
+@pytest.mark.parametrize("regime", ["0.15", "mixed"])
+def test_strong_decay_other_paths(algo, regime):
+    inp = _strong_decay(ssd_synth.make_inputs(W[1], seed=95, batch=2, seqlen=600, nheads=4,
+                                              init_states=True), regime, seed=7)
+    _compare_full(inp, algo)
+
+
+@pytest.mark.parametrize("wi", [1, 3])
+@pytest.mark.parametrize("algo", ALGOS)
+def test_huge_dt_replaces_state(algo, wi):
+    """dt = 50 with A = -1: every token's decay is e^-50, so after each token
+    the state is dt x_t (outer) B_t to well within the tolerance, and y_t is
+    C_t . (dt x_t (outer) B_t) + D x_t."""
+    inp = ssd_synth.make_inputs(W[wi], seed=97, batch=1, seqlen=333, nheads=8, init_states=True)
+    inp["dt"] = torch.full_like(inp["dt"], 50.0)
+    inp["A"] = torch.full((inp["nheads"],), -1.0)
+    ey, ef = _compare_full(inp, algo)
+    y, fin = run_gpu(inp, algo=algo)
+    H, G = inp["nheads"], inp["ngroups"]
+    x = inp["x"].double().numpy()
+    Bm, Cm = inp["B"].double().numpy(), inp["C"].double().numpy()
+    D = inp["D"].double().numpy()
+    for h in range(H):
+        g = h // (H // G)
+        S_last = 50.0 * np.outer(x[0, -1, h], Bm[0, -1, g])
+        assert rel_err(fin[0, h], S_last) <= TOL["bf16"], h
+        y_exp = 50.0 * x[0, :, h] * (Bm[0, :, g] * Cm[0, :, g]).sum(-1)[:, None] + D[h] * x[0, :, h]
+        assert rel_err(y[0, :, h], y_exp) <= TOL["bf16"], h
