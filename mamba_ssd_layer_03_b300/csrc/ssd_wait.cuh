@@ -46,6 +46,9 @@ __device__ __forceinline__ bool fwait(uint64_t *bar, uint32_t parity, int *statu
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
+        // not unrolled: every wait site inlines this loop, and the kernels'
+        // instruction footprint matters more than the loop's few branches
+#pragma unroll 1
         for (int i = 0; i < 16; ++i)
             if (try_wait_sleep(bar, parity, 2000)) return true;
         const uint64_t dt = globaltimer_ns() - t0;
