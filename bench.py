@@ -237,6 +237,28 @@ def time_oracle_sample(inp, budget_s: float):
     return tok_heads / H / elapsed, done, elapsed, threads
 
 
+def oracle_step_budget(steps: int, warmup: int) -> float:
+    """Seconds of oracle work per sample: the reference arm spreads about
+    150 s over its warm-up and timed steps, 1 to 20 s each."""
+    return max(1.0, min(20.0, 150.0 / max(1, steps + warmup)))
+
+
+def oracle_rate(inp, samples: int, warmup: int, budget_s: float):
+    """The oracle's throughput as both arms report it: ``warmup`` untimed
+    samples of ``budget_s`` seconds (the first one also starts the thread
+    pool and touches the inputs), then the mean rate over ``samples`` timed
+    samples of the same budget.  Returns (tokens/s, units, seconds, threads)."""
+    for _ in range(warmup):
+        time_oracle_sample(inp, budget_s)
+    rates, units, secs, threads = [], 0, 0.0, 1
+    for _ in range(max(1, samples)):
+        rate, u, sec, threads = time_oracle_sample(inp, budget_s)
+        rates.append(rate)
+        units += u
+        secs += sec
+    return statistics.mean(rates), units, secs, threads
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -246,14 +268,20 @@ def main():
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--algo", default="auto", choices=["auto", "simt", "tc", "tc2"])
     ap.add_argument("--cpu-budget", type=float, default=12.0,
-                    help="seconds of oracle work for the cpu_baseline leg")
+                    help="about this many seconds of timed oracle work for the cpu_baseline "
+                         "leg (at least one sample of the reference arm's per-step budget)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=None,
                     help="seconds of oracle work per step of --impl reference (default: the "
                          "run's 150 s spread over its steps, 1 to 20 s each)")
     ap.add_argument("--seqlen", type=int, default=None,
                     help="override the workload's tokens per sequence (profiling captures)")
-    ap.add_argument("--op", default="scan", choices=["scan", "step"])
+    ap.add_argument("--dt-softplus", action="store_true",
+                    help="pass the raw step sizes and let the scan apply dt' = softplus(dt + "
+                         "bias) (the step-size transform) as it reads them")
+    ap.add_argument("--op", default="scan", choices=["scan", "step", "seqpar"])
+    ap.add_argument("--shards", type=int, default=2,
+                    help="shards per sequence (--op seqpar)")
     ap.add_argument("--step-batch", type=int, default=64,
                     help="sequences per decode step (--op step)")
     args = ap.parse_args()
@@ -267,6 +295,8 @@ def main():
         return run_reference(args, w, rank, world)
     if args.op == "step":
         return run_step_bench(args, w, rank, world, local)
+    if args.op == "seqpar":
+        return run_seqpar_bench(args, w, rank, world, local)
 
     dist = None
     if world > 1:
@@ -283,15 +313,20 @@ def main():
                            inp["dstate"], inp["ngroups"], inp["chunk"], inp["nseq"],
                            d["x"].dtype, args.algo)
     algo = ssd.resolve_algo(shape)
-    ws = torch.empty(ssd.workspace_size(shape), dtype=torch.uint8, device=dev)
+    # with --dt-softplus the scan reads the raw step sizes and the per-head
+    # bias and applies the transform itself
+    tfk = dict(dt_bias=d["dt_bias"], dt_softplus=True) if args.dt_softplus else {}
+    dt_key = "dt_raw" if args.dt_softplus else "dt"
+    ws = torch.empty(ssd.workspace_size(shape, ssd.make_dt_transform(**tfk)), dtype=torch.uint8,
+                     device=dev)
     y = torch.empty_like(d["x"])
     fin = torch.empty(inp["nseq"], inp["nheads"], inp["headdim"], inp["dstate"],
                       dtype=torch.float32, device=dev)
 
     def step():
-        ssd.ssd_scan(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], inp["chunk"],
+        ssd.ssd_scan(d["x"], d[dt_key], d["A"], d["B"], d["C"], d["D"], inp["chunk"],
                      d["initial_states"], d["cu_seqlens"], True, args.algo, out=y,
-                     final_out=fin, workspace=ws)
+                     final_out=fin, workspace=ws, **tfk)
 
     stream = torch.cuda.current_stream(dev)
     # Warm-up (also checks the device status word once).
@@ -369,7 +404,8 @@ def main():
     e2e = None
     if rank == 0 or world > 1:
         host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-        in_keys = ("x", "dt", "A", "B", "C", "D", "initial_states", "cu_seqlens")
+        in_keys = ("x", dt_key, "A", "B", "C", "D", "initial_states", "cu_seqlens") + (
+            ("dt_bias",) if tfk else ())
         h2d = sum(host[k].numel() * host[k].element_size() for k in in_keys if host[k] is not None)
         y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
         fin_host = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
@@ -380,9 +416,10 @@ def main():
             for k in in_keys:
                 if host[k] is not None:
                     dbuf[k].copy_(host[k], non_blocking=True)
-            ssd.ssd_scan(dbuf["x"], dbuf["dt"], dbuf["A"], dbuf["B"], dbuf["C"], dbuf["D"],
+            tf_e2e = dict(dt_bias=dbuf["dt_bias"], dt_softplus=True) if tfk else {}
+            ssd.ssd_scan(dbuf["x"], dbuf[dt_key], dbuf["A"], dbuf["B"], dbuf["C"], dbuf["D"],
                          inp["chunk"], dbuf["initial_states"], dbuf["cu_seqlens"], True,
-                         args.algo, out=y, final_out=fin, workspace=ws)
+                         args.algo, out=y, final_out=fin, workspace=ws, **tf_e2e)
             y_host.copy_(y, non_blocking=True)
             fin_host.copy_(fin, non_blocking=True)
 
@@ -403,10 +440,15 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, units, secs, threads = time_oracle_sample(inp, args.cpu_budget)
+        # the reference arm's procedure and per-sample budget, fewer samples
+        budget = oracle_step_budget(args.steps, args.warmup)
+        nsamp = max(1, int(round(args.cpu_budget / budget)))
+        rate, units, secs, threads = oracle_rate(inp, nsamp, 1, budget)
         cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"{units} of {inp['nseq'] * inp['nheads']} (sequence, head) units of "
-                         f"the same workload, full length, fp64 recurrence, {secs:.1f} s; "
+               "sample": f"1 warm-up + {nsamp} timed samples of {budget:.3g} s each (the "
+                         f"reference arm's per-step budget for these --steps/--warmup): "
+                         f"{units} (sequence, head) units of the same workload in total, full "
+                         f"length, fp64 recurrence, {secs:.1f} s timed; mean of the samples' "
                          f"tokens/s = unit-tokens / nheads / seconds"}
 
     if rank == 0:
@@ -443,8 +485,11 @@ def main():
         }
         if args.seqlen is not None:
             out["config"]["seqlen_override"] = args.seqlen
-        out["gpu_launches"] = launches_per_step(
-            algo, inp, torch.cuda.get_device_properties(dev).multi_processor_count) * args.steps
+        if tfk:
+            out["config"]["dt_transform"] = "dt' = softplus(dt + bias), applied by the scan"
+        out["gpu_launches"] = (launches_per_step(
+            algo, inp, torch.cuda.get_device_properties(dev).multi_processor_count)
+            + (1 if tfk and algo != "tc" else 0)) * args.steps
         print(json.dumps(out))
     if dist:
         dist.destroy_process_group()
@@ -599,6 +644,95 @@ def run_step_bench(args, w, rank, world, local):
         dist.destroy_process_group()
 
 
+def run_seqpar_bench(args, w, rank, world, local):
+    """Device work of one rank of the sequence-parallel scan (seqpar.py): the
+    last of ``--shards`` consecutive shards of every sequence of workload w,
+    which folds the most carries.  A step is the scan of the shard from a
+    zero state, its log-decay, the fold of all shards' carries into its entry
+    state and the final state, and the re-scan from the entry state.  The
+    all_gather is not in the step (one GPU: there is no peer); the other
+    shards' carries are stand-ins of the right size, and the rank's own carry
+    is copied into its slot as the collective would place it."""
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from mamba_ssd_layer_03_b300 import seqpar
+    R = max(1, args.shards)
+    Ls = w.seqlen // R
+    inp = ssd_synth.make_inputs(w, seed=rank, seqlen=Ls, init_states=True)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    b, H, P, N = inp["batch"], inp["nheads"], inp["headdim"], inp["dstate"]
+    g = torch.Generator(device=dev).manual_seed(7)
+    S_all = torch.randn(R, b, H, P, N, generator=g, device=dev) * 0.1
+    ld_all = -torch.rand(R, b, H, generator=g, device=dev) * 4.0
+    ops = seqpar.CudaOps(args.algo)
+    y = torch.empty_like(d["x"])
+    me = R - 1
+    import mamba_ssd_layer_03_b300 as ssd
+    algo = ssd.resolve_algo(ssd.make_shape(b, Ls, H, P, N, inp["ngroups"], inp["chunk"], b,
+                                           d["x"].dtype, args.algo))
+    launches = 2 * launches_per_step(algo, inp, torch.cuda.get_device_properties(dev)
+                                     .multi_processor_count) + 2
+
+    def step():
+        _, S = ops.scan(d["x"], d["dt"], d["A"], d["B"], d["C"], None, inp["chunk"], None, out=y)
+        ld = ops.logdec(d["dt"], d["A"])
+        S_all[me].copy_(S)
+        ld_all[me].copy_(ld)
+        entry, fin = ops.fold(S_all, ld_all, me, d["initial_states"])
+        ops.scan(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], inp["chunk"], entry, out=y,
+                 final=False)
+        return fin
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(local)
+    with sampler:
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_host0 = time.perf_counter()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        t_host1 = time.perf_counter()
+        time.sleep(0.15)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    scan_bytes, _, _ = workload_cost(inp)
+    state = b * H * P * N * 4
+    # two scans (the first without D and initial states), the log-decay's dt
+    # read, the fold's R carries read, initial states read, entry and final
+    # states written
+    nbytes = 2 * scan_bytes + b * Ls * H * 4 + R * (state + b * H * 4) + 3 * state
+    peaks = load_peaks()
+    if rank == 0:
+        out = {
+            "metric": "SSD sequence-parallel scan, one rank's device work, shard tokens/s on 1 B300",
+            "value": b * Ls / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": inp["dtype"],
+            "data": "synthetic (seeded, the workload's distributions)",
+            "config": {"workload": f"{w.name}_shard{R - 1}of{R}", "batch": b, "shard_seqlen": Ls,
+                       "nheads": H, "headdim": P, "dstate": N, "algo": algo,
+                       "launch": "eager (four library calls per step)",
+                       "collective": "not timed: one GPU, no peers; the other shards' carries "
+                                     "are stand-ins"},
+            "roofline": {"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": nbytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                         "traffic": None, "peak_source": peaks["source"],
+                         "kernel": "two scans + k_shard_logdec + k_carry_fold (whole step)",
+                         "algorithmic_bytes": nbytes, "kernel_ms": ms},
+            "cpu_baseline": None, "e2e": None,
+            "gpu_launches": launches * args.steps,
+            "clocks": sampler.summary(t_host0, t_host1),
+        }
+        print(json.dumps(out))
+
+
 def fused_splits_lanes(inp, sms):
     """Whether the fused kernel splits lanes between CTAs (its two-run mode):
     at most half as many lanes as SMs, at least 16 blocks per lane, no
@@ -628,17 +762,8 @@ def run_reference(args, w, rank, world):
         return
     import oracle
     inp = ssd_synth.make_inputs(w, seed=0)
-    budget = args.ref_budget if args.ref_budget else max(
-        1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
-    for _ in range(args.warmup):
-        time_oracle_sample(inp, budget)
-    rates, secs_total, units_total = [], 0.0, 0
-    for _ in range(args.steps):
-        rate, units, secs, threads = time_oracle_sample(inp, budget)
-        rates.append(rate)
-        secs_total += secs
-        units_total += units
-    value = statistics.mean(rates)
+    budget = args.ref_budget if args.ref_budget else oracle_step_budget(args.steps, args.warmup)
+    value, _, _, threads = oracle_rate(inp, args.steps, args.warmup, budget)
     tokens = inp["batch"] * inp["seqlen"]
     sample = (f"each step: about {budget:.3g} s of (sequence, head) units of the same workload "
               f"(full length, fp64 recurrence); tokens/s = unit-tokens / nheads / seconds")

@@ -257,6 +257,64 @@ SSD_API const char *ssd_status_string(int status);
 SSD_API int ssd_resolve_algo(const ssd_shape *shape);
 
 /*
+ * Sequence parallelism: the carry exchange between shards of a sequence
+ * (QbitAI article "新架构Mamba更新二代！", section "Mamba-2：更强学习能力，
+ * 更快训练推理": sequence parallelism for longer sequences).  Every sequence
+ * is cut into nshards consecutive pieces, shard r on device r.  The state is
+ * the only thing that crosses a cut.  Each device scans its shard from a zero
+ * state (ssd_scan(), final_states -> S_r) and computes its shard's log-decay
+ *     logdec_r[s, h] = sum over the shard's tokens t of sequence s of dt'_t A_h
+ * (ssd_seqpar_logdec).  The devices all-gather (S_r, logdec_r); each folds
+ *     H_in(0)     = initial_states (or zero)
+ *     H_in(q + 1) = exp(logdec_q) H_in(q) + S_q
+ * (ssd_seqpar_fold) and re-scans its shard from H_in(r), which gives its part
+ * of y exactly as the unsharded scan would; H_in(nshards) is the sequence's
+ * final state.  This is the chunk-to-chunk state passing of the block
+ * decomposition, one step per shard.
+ */
+
+/*
+ * logdec[s][h] (fp32, DEVICE, [batch][nheads], caller-owned) for the shard
+ * in `shape`'s layout: sequence s is batch row s (nseq == batch; packed
+ * sequences are not sharded), and only batch, seqlen, nheads and nseq are
+ * used (plus ssd_scan()'s size checks).  dt [batch][seqlen][nheads] and A
+ * [nheads] are fp32 DEVICE pointers; dt_transform as for ssd_scan_ex()
+ * (nullable).  seqlen 0 gives 0 (dt may then be NULL).  Sums in fp64, stores
+ * fp32.  Errors on the host
+ * before anything is enqueued: SSD_ERR_INVALID_ARG (null pointer, bad
+ * shape), SSD_ERR_UNSUPPORTED (misaligned fp32 pointer, shape too large);
+ * SSD_ERR_CUDA if the launch fails.  Asynchronous on `stream`; allocates
+ * nothing.
+ */
+SSD_API int ssd_seqpar_logdec(const ssd_shape *shape, const float *dt,
+                              const ssd_dt_transform *dt_transform, const float *A,
+                              float *logdec, void *stream);
+
+/*
+ * The fold over shards, for shard `rank` of `nshards`.  All fp32 DEVICE
+ * pointers owned by the caller:
+ *   shard_states          [nshards][nseq][nheads][headdim][dstate]: S_q,
+ *                         each shard's state scanned from zero (gathered)
+ *   shard_logdec          [nshards][nseq][nheads]: logdec_q (gathered)
+ *   initial_states        [nseq][nheads][headdim][dstate], nullable (zero)
+ *   shard_initial_states  [nseq][nheads][headdim][dstate]: H_in(rank),
+ *                         nullable (not written)
+ *   final_states          [nseq][nheads][headdim][dstate]: H_in(nshards),
+ *                         nullable (not written); at least one of the two
+ *                         outputs is required
+ * Outputs must not overlap inputs.  Errors on the host before anything is
+ * enqueued: SSD_ERR_INVALID_ARG (rank outside [0, nshards), sizes < 1, nseq
+ * < 0, missing pointer), SSD_ERR_UNSUPPORTED (misaligned pointer, over 2^56
+ * elements); SSD_ERR_CUDA if the launch fails.  Asynchronous on `stream`;
+ * allocates nothing.
+ */
+SSD_API int ssd_seqpar_fold(int32_t nshards, int32_t rank, int64_t nseq, int32_t nheads,
+                            int32_t headdim, int32_t dstate, const float *shard_states,
+                            const float *shard_logdec, const float *initial_states,
+                            float *shard_initial_states, float *final_states,
+                            void *stream);
+
+/*
  * ssd_scan() without a workspace: for callers that cannot allocate device
  * memory when they run the scan -- code running inside another framework's
  * execution hook (an inference runtime's plugin enqueue, a custom-op

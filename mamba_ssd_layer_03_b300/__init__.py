@@ -107,6 +107,12 @@ def load_library() -> ctypes.CDLL:
     lib.ssd_step.restype = ctypes.c_int
     lib.ssd_selftest_wait_timeout.argtypes = [ctypes.c_int, vp, vp]
     lib.ssd_selftest_wait_timeout.restype = ctypes.c_int
+    lib.ssd_seqpar_logdec.argtypes = [sp, vp, tp, vp, vp, vp]
+    lib.ssd_seqpar_logdec.restype = ctypes.c_int
+    i32 = ctypes.c_int32
+    lib.ssd_seqpar_fold.argtypes = [i32, i32, ctypes.c_int64, i32, i32, i32, vp, vp, vp, vp, vp,
+                                    vp]
+    lib.ssd_seqpar_fold.restype = ctypes.c_int
     _lib = lib
     return lib
 

@@ -8,7 +8,8 @@
 // "Mamba-2：更强学习能力，更快训练推理" for the block-decomposition algorithm):
 //
 //   K1 chunk cumsum   cs_i = sum of a_k = dt_k A_h over the chunk, restarted
-//                     at every packed-sequence start inside the chunk (fp64)
+//                     at every packed-sequence start inside the chunk (fp64,
+//                     a warp-wide segmented scan per head)
 //   K2 chunk state    S_c = sum_j exp(cs_last - cs_j) dt_j x_j (outer) B_j over
 //                     the chunk's last sequence piece, from a zero state
 //   K3 state passing  E_c (state entering chunk c's first sequence piece):
@@ -60,25 +61,54 @@ __device__ __forceinline__ int64_t seq_start(const KArgs &a, int s) {
     return a.varlen ? (int64_t)__ldg(a.cu + s) : 0;
 }
 
-// K1: grid (nc, batch), block 128; one thread per head walks its chunk.
-__global__ void k1_chunk_cumsum(KArgs a) {
+// K1: grid (nc, batch, ceil(H / 32)), block kK1Threads.  The chunk's dt for
+// 32 heads is staged in shared memory with coalesced reads (32 consecutive
+// heads of one token per warp load); then each warp takes whole heads, 32
+// tokens per step: a warp-wide segmented inclusive scan in fp64 (a segment
+// starts where a packed sequence starts), plus the running sum carried from
+// the previous 32 tokens, written to cs as 32 consecutive doubles.
+constexpr int kK1Threads = 256;
+constexpr int kMaxQ = 256;
+
+__global__ void __launch_bounds__(kK1Threads) k1_chunk_cumsum(KArgs a) {
+    __shared__ float tile[kMaxQ][33];   // [token][head]; 33: no bank conflicts
+    __shared__ int seg[kMaxQ];          // packed-sequence index of each token
     if (status_bad(a.status)) return;
-    const int c = blockIdx.x, r = blockIdx.y;
+    const int c = blockIdx.x, r = blockIdx.y, hb = blockIdx.z * 32;
     const int64_t t0 = (int64_t)c * a.Q;
     const int len = (int)min64(a.Q, a.L - t0);
-    for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
+    const int nh = min(32, a.H - hb);
+    for (int idx = threadIdx.x; idx < len * 32; idx += kK1Threads) {
+        const int i = idx >> 5, hl = idx & 31;
+        if (hl < nh) tile[i][hl] = __ldg(a.dt + ((int64_t)r * a.L + t0 + i) * a.H + hb + hl);
+    }
+    if (a.varlen)
+        for (int i = threadIdx.x; i < len; i += kK1Threads) seg[i] = seg_of(a.cu, a.nseq, t0 + i);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int hl = warp; hl < nh; hl += kK1Threads / 32) {
+        const int h = hb + hl;
         const double Ah = (double)__ldg(a.A + h);
-        double run = 0.0;
-        int cur = seq_of(a, r, t0);
         double *out = a.cs + cs_index(a, r, h, c);
-        for (int i = 0; i < len; ++i) {
-            const int64_t t = t0 + i;
-            if (a.varlen) {
-                int s = seg_of(a.cu, a.nseq, t);
-                if (s != cur) { cur = s; run = 0.0; }
+        double carry = 0.0;
+        for (int i0 = 0; i0 < len; i0 += 32) {
+            const int i = i0 + lane;
+            const bool valid = i < len;
+            double v = valid ? (double)tile[i][hl] * Ah : 0.0;
+            // f: a segment starts at or before this lane within these 32 tokens
+            int f = (a.varlen && valid && i > 0 && seg[i] != seg[i - 1]) ? 1 : 0;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const double vv = __shfl_up_sync(0xffffffffu, v, d);
+                const int ff = __shfl_up_sync(0xffffffffu, f, d);
+                if (lane >= d) {
+                    if (!f) v += vv;
+                    f |= ff;
+                }
             }
-            run += (double)__ldg(a.dt + ((int64_t)r * a.L + t) * a.H + h) * Ah;
-            out[i] = run;
+            const double run = f ? v : carry + v;
+            if (valid) out[i] = run;
+            carry = __shfl_sync(0xffffffffu, run, 31);
         }
     }
 }
@@ -289,7 +319,7 @@ cudaError_t launch_all(const Problem &p) {
     a.S = (float *)(p.ws + w.S);
     a.E = (float *)(p.ws + w.E);
     const unsigned b = (unsigned)p.batch;
-    k1_chunk_cumsum<<<dim3(p.nc, b), 128, 0, p.stream>>>(a);
+    k1_chunk_cumsum<<<dim3(p.nc, b, (p.H + 31) / 32), kK1Threads, 0, p.stream>>>(a);
     k2_chunk_state<T><<<dim3(p.nc, b, p.H), 256, p.Q * sizeof(float), p.stream>>>(a);
     const int PN = p.P * p.N;
     k3_state_passing<<<dim3((PN + 255) / 256, p.H, b), 256, 0, p.stream>>>(a);
@@ -306,7 +336,7 @@ size_t simt_workspace_bytes(const Problem &p) { return layout(p).total; }
 
 int simt_supported(const Problem &p) {
     if (p.P < 1 || p.P > 256 || p.N < 1 || p.N > 256) return SSD_ERR_UNSUPPORTED;
-    if (p.Q != 64 && p.Q != 128 && p.Q != 256) return SSD_ERR_UNSUPPORTED;
+    if (p.Q != 64 && p.Q != 128 && p.Q != 256) return SSD_ERR_UNSUPPORTED;   // <= kMaxQ
     if (p.dtype != SSD_F32 && p.dtype != SSD_BF16) return SSD_ERR_UNSUPPORTED;
     return SSD_OK;
 }
