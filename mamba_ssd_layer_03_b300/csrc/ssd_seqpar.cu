@@ -15,73 +15,102 @@
 // that exchange; the scans are ssd_scan().
 #include <cuda_runtime.h>
 
+#include <cooperative_groups.h>
+
 #include "ssd_device.cuh"
 #include "ssd_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace ssd {
 namespace {
 
-constexpr int kLogdecThreads = 1024;
+constexpr int kLogdecThreads = 256;
 constexpr int kLogdecWarps = kLogdecThreads / 32;
+constexpr int kLogdecCluster = 8;                    // CTAs per (sequence, head block)
+constexpr int kLogdecStride = kLogdecWarps * kLogdecCluster;   // warps over one token range
+constexpr int kLogdecRun = 16;                       // tokens summed in fp32 before fp64
 
-// logdec[s][h] = sum_t dt'[s, t, h] A_h over the L tokens of batch row s
-// (sequence s's tokens on this shard).  CTA (s, 32-head block); warp w takes
-// tokens t = w, w + 32, ..., lane = head, so that every load of a warp reads
-// 32 consecutive heads of one token.  Sums in fp64, in a fixed order (four
-// running sums per thread, then the warps in order): exp(logdec) enters
-// every later shard's state, and the result does not depend on timing.
-__global__ void __launch_bounds__(kLogdecThreads) k_shard_logdec(const float *dt, const float *A,
-                                                                 int64_t L, int H, DtTransform tf,
-                                                                 float *logdec) {
+// logdec[s][h] = A_h * sum_t dt'[s, t, h] over the L tokens of batch row s
+// (sequence s's tokens on this shard; A_h is the same for every token, so
+// it multiplies the sum once).  A cluster of kLogdecCluster CTAs takes one
+// (sequence, 32-head block): warp w of CTA z takes tokens t = z * 8 + w,
+// then every 64th token, lane = head, so that every load of a warp reads 32
+// consecutive heads of one token.  Each thread sums runs of 16 tokens in
+// fp32 and adds the runs in fp64; the CTA adds its warps in order, and CTA 0
+// of the cluster adds the CTAs in order through distributed shared memory.
+// The result does not depend on timing.
+__global__ void __cluster_dims__(1, 1, kLogdecCluster) __launch_bounds__(kLogdecThreads)
+    k_shard_logdec(const float *__restrict__ dt, const float *__restrict__ A, int64_t L, int H,
+                   DtTransform tf, float *__restrict__ logdec) {
     __shared__ double part[kLogdecWarps][32];
+    __shared__ double cta_sum[32];
+    cg::cluster_group cluster = cg::this_cluster();
     const int s = blockIdx.x;
+    const int z = (int)cluster.block_rank();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y * 32 + lane;
-    double acc[4] = {0.0, 0.0, 0.0, 0.0};
+    double acc = 0.0;
     if (h < H) {
-        const float a = __ldg(A + h);
         const float bias = tf.bias ? __ldg(tf.bias + h) : 0.f;
         const float *row = dt + (int64_t)s * L * H + h;
-        int64_t t = warp;
-        for (; t + 3 * kLogdecWarps < L; t += 4 * kLogdecWarps) {
-            float d[4];
+        int64_t t = z * kLogdecWarps + warp;
+        // full runs: all 16 loads in flight before the sum
+        for (; t + (kLogdecRun - 1) * kLogdecStride < L; t += kLogdecRun * kLogdecStride) {
+            float d[kLogdecRun];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) d[k] = __ldg(row + (t + k * kLogdecWarps) * H);
+            for (int k = 0; k < kLogdecRun; ++k) d[k] = __ldg(row + (t + k * kLogdecStride) * H);
+            float run = 0.f;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < kLogdecRun; ++k) {
                 if (tf.on) d[k] = dt_apply(d[k], bias, tf.softplus, tf.lo, tf.hi);
-                acc[k] += (double)d[k] * (double)a;
+                run += d[k];
             }
+            acc += (double)run;
         }
-        for (; t < L; t += kLogdecWarps) {
+        float run = 0.f;   // the last, partial run
+        for (; t < L; t += kLogdecStride) {
             float d = __ldg(row + t * H);
             if (tf.on) d = dt_apply(d, bias, tf.softplus, tf.lo, tf.hi);
-            acc[0] += (double)d * (double)a;
+            run += d;
         }
+        acc += (double)run;
     }
-    part[warp][lane] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    part[warp][lane] = acc;
     __syncthreads();
-    if (warp == 0 && h < H) {
+    if (warp == 0) {
         double sum = 0.0;
-#pragma unroll 8
+#pragma unroll
         for (int w = 0; w < kLogdecWarps; ++w) sum += part[w][lane];
-        logdec[(int64_t)s * H + h] = (float)sum;
+        cta_sum[lane] = sum;
     }
+    cluster.sync();   // every CTA's cta_sum is written
+    if (z == 0 && warp == 0 && h < H) {
+        double sum = 0.0;
+#pragma unroll
+        for (int q = 0; q < kLogdecCluster; ++q) sum += cluster.map_shared_rank(cta_sum, q)[lane];
+        logdec[(int64_t)s * H + h] = (float)(sum * (double)__ldg(A + h));
+    }
+    cluster.sync();   // keep every CTA's shared memory alive until CTA 0 has read it
 }
 
-// The fold over shards, one state element per thread: e runs over
-// (sequence, head, p, n), sh = e / PN is its (sequence, head).
+// The fold over shards, one state element per thread (four with float4 when
+// the state rows and every pointer allow): e runs over (sequence, head, p,
+// n), sh = e / PN is its (sequence, head).
 //   H = init (or 0); for q = 0 .. nshards - 1:
 //       (q == rank: h_in = H);  H = exp(logdec_q) H + S_q
 //   total = H
-__global__ void k_carry_fold(const float *S_all, const float *logdec_all, const float *init,
-                             int nshards, int rank, int64_t nsh, int64_t PN, float *h_in,
-                             float *total) {
+// No load depends on the running H, so the S_q of the next shards are in
+// flight while the multiply-adds run.
+__global__ void k_carry_fold(const float *__restrict__ S_all, const float *__restrict__ logdec_all,
+                             const float *__restrict__ init, int nshards, int rank, int64_t nsh,
+                             int64_t PN, float *__restrict__ h_in, float *__restrict__ total) {
     const int64_t n = nsh * PN;
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
          e += (int64_t)gridDim.x * blockDim.x) {
         const int64_t sh = e / PN;
         float Hs = init ? __ldg(init + e) : 0.f;
+#pragma unroll 4
         for (int q = 0; q < nshards; ++q) {
             if (q == rank && h_in) h_in[e] = Hs;
             const float dq = expf(__ldg(logdec_all + (int64_t)q * nsh + sh));
@@ -91,7 +120,30 @@ __global__ void k_carry_fold(const float *S_all, const float *logdec_all, const 
     }
 }
 
+__global__ void k_carry_fold4(const float4 *__restrict__ S_all, const float *__restrict__ logdec_all,
+                              const float4 *__restrict__ init, int nshards, int rank, int64_t nsh,
+                              int64_t PN4, float4 *__restrict__ h_in, float4 *__restrict__ total) {
+    const int64_t n4 = nsh * PN4;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n4;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t sh = e / PN4;
+        float4 Hs = init ? __ldg(init + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int q = 0; q < nshards; ++q) {
+            if (q == rank && h_in) h_in[e] = Hs;
+            const float dq = expf(__ldg(logdec_all + (int64_t)q * nsh + sh));
+            const float4 Sq = __ldg(S_all + (int64_t)q * n4 + e);
+            Hs.x = fmaf(dq, Hs.x, Sq.x);
+            Hs.y = fmaf(dq, Hs.y, Sq.y);
+            Hs.z = fmaf(dq, Hs.z, Sq.z);
+            Hs.w = fmaf(dq, Hs.w, Sq.w);
+        }
+        if (total) total[e] = Hs;
+    }
+}
+
 bool aligned4(const void *p) { return ((uintptr_t)p % 4) == 0; }
+bool aligned16(const void *p) { return ((uintptr_t)p % 16) == 0; }
 
 }  // namespace
 }  // namespace ssd
@@ -121,7 +173,7 @@ extern "C" SSD_API int ssd_seqpar_logdec(const ssd_shape *s, const float *dt,
         tf.on = true;
     }
     if ((s->nheads + 31) / 32 > 65535) return SSD_ERR_UNSUPPORTED;   // grid.y limit
-    const dim3 grid((unsigned)s->nseq, (unsigned)((s->nheads + 31) / 32));
+    const dim3 grid((unsigned)s->nseq, (unsigned)((s->nheads + 31) / 32), kLogdecCluster);
     k_shard_logdec<<<grid, kLogdecThreads, 0, (cudaStream_t)stream>>>(dt, A, s->seqlen,
                                                                       s->nheads, tf, logdec);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
@@ -144,12 +196,19 @@ extern "C" SSD_API int ssd_seqpar_fold(int32_t nshards, int32_t rank, int64_t ns
         !aligned4(shard_initial_states) || !aligned4(final_states))
         return SSD_ERR_UNSUPPORTED;
     const int64_t nsh = nseq * nheads, PN = (int64_t)headdim * dstate;
-    const int64_t n = nsh * PN;
     const int threads = 256;
+    const bool vec = PN % 4 == 0 && aligned16(shard_states) && aligned16(initial_states) &&
+                     aligned16(shard_initial_states) && aligned16(final_states);
+    const int64_t n = nsh * (vec ? PN / 4 : PN);
     const int64_t want = (n + threads - 1) / threads;
     const unsigned blocks = (unsigned)(want < 148 * 8 ? want : 148 * 8);
-    k_carry_fold<<<blocks, threads, 0, (cudaStream_t)stream>>>(
-        shard_states, shard_logdec, initial_states, nshards, rank, nsh, PN, shard_initial_states,
-        final_states);
+    if (vec)
+        k_carry_fold4<<<blocks, threads, 0, (cudaStream_t)stream>>>(
+            (const float4 *)shard_states, shard_logdec, (const float4 *)initial_states, nshards,
+            rank, nsh, PN / 4, (float4 *)shard_initial_states, (float4 *)final_states);
+    else
+        k_carry_fold<<<blocks, threads, 0, (cudaStream_t)stream>>>(
+            shard_states, shard_logdec, initial_states, nshards, rank, nsh, PN,
+            shard_initial_states, final_states);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

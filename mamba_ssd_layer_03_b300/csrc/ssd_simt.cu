@@ -150,32 +150,68 @@ __global__ void k2_chunk_state(KArgs a) {
 }
 
 // K3: grid (ceil(P*N/256), H, batch), block 256; one thread per state
-// element walks the chunks of its row in order.
-__global__ void k3_state_passing(KArgs a) {
+// element walks the chunks of its row in order.  The walk is a chain of one
+// multiply-add per chunk; what feeds it does not depend on the chain, so it
+// is computed ahead: per group of 32 chunks, lane j of every warp works out
+// chunk c0 + j's decay exp(cs_last) (fp64 exp, once per chunk instead of
+// once per element), its first/last sequence and whether a sequence starts
+// or ends there, and shares them by shuffles; the chunk states S are loaded
+// kK3Ahead chunks at a time before the chain consumes them.
+constexpr int kK3Ahead = 8;
+
+__global__ void __launch_bounds__(256) k3_state_passing(KArgs a) {
     if (status_bad(a.status)) return;
     const int h = blockIdx.y, r = blockIdx.z;
     const int PN = a.P * a.N;
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= PN) return;
+    const bool live = e < PN;            // dead lanes still take part in the shuffles
+    const int lane = threadIdx.x & 31;
+    const float *S = a.S + st_index(a, r, 0, h) + e;
+    float *E = a.E + st_index(a, r, 0, h) + e;
+    const int64_t cstride = (int64_t)a.H * PN;   // from chunk c to c + 1 in S and E
+    const float *init = a.init ? a.init + (int64_t)h * PN + e : nullptr;   // + seq * H * PN
+    float *fin = a.final_states ? a.final_states + (int64_t)h * PN + e : nullptr;
     float end_state = 0.f;
-    for (int c = 0; c < a.nc; ++c) {
-        const int64_t t0 = (int64_t)c * a.Q;
-        const int len = (int)min64(a.Q, a.L - t0);
-        const int fs = seq_of(a, r, t0);
-        const int ls = seq_of(a, r, t0 + len - 1);
-        float E;
-        if (c == 0 || seq_start(a, fs) == t0)   // a sequence starts here
-            E = a.init ? a.init[((int64_t)fs * a.H + h) * PN + e] : 0.f;
-        else
-            E = end_state;                      // carried across the boundary
-        a.E[st_index(a, r, c, h) + e] = E;
-        float El = (ls == fs) ? E : (a.init ? a.init[((int64_t)ls * a.H + h) * PN + e] : 0.f);
-        const double cl = a.cs[cs_index(a, r, h, c) + len - 1];
-        end_state = (float)exp(cl) * El + a.S[st_index(a, r, c, h) + e];
-        const int64_t t_end = t0 + len - 1;
-        const int64_t seq_last = a.varlen ? (int64_t)__ldg(a.cu + ls + 1) - 1 : a.L - 1;
-        if (a.final_states && seq_last == t_end)
-            a.final_states[((int64_t)ls * a.H + h) * PN + e] = end_state;
+    for (int c0 = 0; c0 < a.nc; c0 += 32) {
+        // per-chunk facts, chunk c0 + lane
+        float dec_l = 0.f;
+        int fs_l = 0, ls_l = 0, flags_l = 0;   // bit 0: sequence starts; bit 1: final here
+        const int cl_ = c0 + lane;
+        if (cl_ < a.nc) {
+            const int64_t t0 = (int64_t)cl_ * a.Q;
+            const int len = (int)min64(a.Q, a.L - t0);
+            fs_l = seq_of(a, r, t0);
+            ls_l = seq_of(a, r, t0 + len - 1);
+            dec_l = (float)exp(a.cs[cs_index(a, r, h, cl_) + len - 1]);
+            if (cl_ == 0 || seq_start(a, fs_l) == t0) flags_l |= 1;
+            const int64_t seq_last = a.varlen ? (int64_t)__ldg(a.cu + ls_l + 1) - 1 : a.L - 1;
+            if (seq_last == t0 + len - 1) flags_l |= 2;
+        }
+        const int ng = min(32, a.nc - c0);
+        for (int j0 = 0; j0 < ng; j0 += kK3Ahead) {
+            float Sv[kK3Ahead];
+#pragma unroll
+            for (int k = 0; k < kK3Ahead; ++k)
+                Sv[k] = (live && j0 + k < ng) ? S[(int64_t)(c0 + j0 + k) * cstride] : 0.f;
+#pragma unroll
+            for (int k = 0; k < kK3Ahead; ++k) {
+                const int j = j0 + k;
+                const float dec = __shfl_sync(0xffffffffu, dec_l, j & 31);
+                const int fs = __shfl_sync(0xffffffffu, fs_l, j & 31);
+                const int ls = __shfl_sync(0xffffffffu, ls_l, j & 31);
+                const int flags = __shfl_sync(0xffffffffu, flags_l, j & 31);
+                if (j < ng && live) {
+                    const int64_t c = c0 + j;
+                    float Ec = end_state;   // carried across the boundary
+                    if (flags & 1) Ec = init ? init[(int64_t)fs * a.H * PN] : 0.f;
+                    E[c * cstride] = Ec;
+                    const float El =
+                        (ls == fs) ? Ec : (init ? init[(int64_t)ls * a.H * PN] : 0.f);
+                    end_state = dec * El + Sv[k];
+                    if (fin && (flags & 2)) fin[(int64_t)ls * a.H * PN] = end_state;
+                }
+            }
+        }
     }
 }
 

@@ -110,7 +110,8 @@ def fold_carries(shard_states: torch.Tensor, shard_logdec_all: torch.Tensor, ran
 
 
 class CudaOps:
-    """The three device steps of the exchange, on the library's kernels."""
+    """The three device steps of the exchange on the library's kernels, and
+    the all-gather on the tensors' device."""
 
     def __init__(self, algo: str = "auto", dt_bias=None, dt_softplus=False, dt_limit=None):
         self.algo = algo
