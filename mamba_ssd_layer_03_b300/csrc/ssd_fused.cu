@@ -35,24 +35,28 @@
 //   M_h  = CB o exp(cs_h[i] - cs_h[j]) dt_h[j] [j <= i] + D_h [i == j]
 //                                                   CUDA cores, TMEM (bf16)
 //   acc_h = exp(cs_h[i]) Ys_h + M_h x_h            tensor cores (A from TMEM)
-//   y_h  = acc_h                                    -> shared memory -> TMA store
+//   y_h  = acc_h                                    -> x tiles (smem) -> TMA store
 // Every exponent is <= 0.  Adding D_h on the diagonal of M_h folds the skip
 // term D_h x_h into the same product.  The masked block is factored at
 // 32-token sub-blocks: for j in an earlier sub-block with last token e,
 // exp(cs_i - cs_j) = exp(cs_i - cs_e) exp(cs_e - cs_j), so only the sub-block
 // holding i needs one exponential per element.
 //
-// Roles (320 threads, one CTA per SM).  Warps 0-3 and 4-7 are two
+// Roles (512 threads, one CTA per SM).  Warps 0-3 and 4-7 are two
 // warpgroups that each cover all 128 TMEM lanes (thread index within the
 // warpgroup = TMEM lane).  Narrow lanes: warpgroup h holds head h for the
-// scan, the state and y, and columns [64 h, 64 h + 64) of C B^T for the mask.
+// scan and the state, and columns [64 h, 64 h + 64) of C B^T for the mask.
 // Wide lanes: both scan the one head; warpgroup h holds state rows
-// [128 h, 128 h + 128), half of each row of Xw and y, and the same column half
-// of C B^T.  Warp 8 issues the TMA loads and writes a descriptor of each block
+// [128 h, 128 h + 128), half of each row of Xw, and the same column half of
+// C B^T.  Warp 8 issues the TMA loads and writes a descriptor of each block
 // (lane, tokens, flags, A, D) into a small shared-memory ring; warp 9 issues
-// the MMAs.  They hand work to each other through mbarriers; every wait is
-// bounded in time and, once the call's status word records an error, falls
-// through so that the kernel always finishes.
+// the MMAs; warps 12-15 (a third warpgroup over the 128 TMEM lanes) take y
+// of each finished block out of TMEM, stage it in the block's x tiles and
+// store it with TMA, so that the compute warps go straight on to the next
+// block.  Warps 10 and 11 only complete the warpgroup of warps 8 and 9.  The
+// roles hand work to each other through mbarriers; every wait is bounded in
+// time and, once the call's status word records an error, falls through so
+// that the kernel always finishes.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -70,7 +74,22 @@ using namespace wait;
 typedef __nv_bfloat16 bf16;
 
 constexpr int kB = 128;                    // tokens per block
-constexpr int kThreads = 320;              // 8 compute warps + TMA warp + MMA warp
+constexpr int kThreads = 512;              // 8 compute warps, TMA warp, MMA warp, 2 idle, 4 epilogue
+// Register split (setmaxnreg).  The kernel is launched with kRegLaunch
+// registers per thread (ptxas gives 128 to 512 threads on one SM); the TMA
+// and MMA warpgroup (warps 8-11) gives registers back down to kRegProducer,
+// the epilogue warpgroup (warps 12-15) down to kRegEpilogue, and the two
+// compute warpgroups take them up to kRegCompute.  Each SM sub-partition
+// holds one warp of each warpgroup: 2 x 168 + 88 + 88 = 512 registers per
+// lane, exactly its share; the host launches the kernel only when ptxas gave
+// it kRegLaunch, so that the increase is always granted.
+constexpr int kRegLaunch = 128;
+constexpr int kRegCompute = 168;
+constexpr int kRegProducer = 88;    // TMA and MMA warpgroup (warps 8-11)
+constexpr int kRegEpilogue = 88;    // epilogue warpgroup (warps 12-15)
+static_assert(2 * 128 * kRegCompute + 128 * kRegProducer + 128 * kRegEpilogue <= kThreads * kRegLaunch,
+              "register split");
+static_assert(2 * kRegCompute + kRegProducer + kRegEpilogue <= 512, "register split per sub-partition");
 constexpr uint32_t kT16 = 16384;           // one 128-row x 128-byte swizzled tile
 constexpr int kP = 64;                     // headdim of this path
 constexpr int kStateFloats = 2 * kP * 128; // state of one lane: 2 heads x 128 or 1 head x 256
@@ -147,7 +166,7 @@ struct Smem {
     uint64_t c_full, b_full, x_full[2];
     uint64_t cb_done, s_done, mx_done[2], c_empty, b_empty, x_empty[2], mma_fin;
     uint64_t hop_ready, xw_ready, m_ready, acc_free[2];
-    uint64_t desc_full[kDescRing];
+    uint64_t desc_full[kDescRing], desc_free[kDescRing];
     BDesc desc[kDescRing];
     uint32_t tmem;
     int ticket;
@@ -274,6 +293,16 @@ __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// Warpgroup register reallocation; every warp of the warpgroup executes it.
+template <uint32_t N>
+__device__ __forceinline__ void regs_up() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_down() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Plain bounded wait used only while draining at exit.
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
@@ -391,8 +420,11 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         mbar_init(&sm->mma_fin, 1);
         mbar_init(&sm->hop_ready, 256); mbar_init(&sm->xw_ready, 256);
         mbar_init(&sm->m_ready, 256);
-        mbar_init(&sm->acc_free[0], 256); mbar_init(&sm->acc_free[1], 256);
-        for (int r = 0; r < kDescRing; ++r) mbar_init(&sm->desc_full[r], 1);
+        mbar_init(&sm->acc_free[0], 128); mbar_init(&sm->acc_free[1], 128);
+        for (int r = 0; r < kDescRing; ++r) {
+            mbar_init(&sm->desc_full[r], 1);
+            mbar_init(&sm->desc_free[r], 128);
+        }
         fence_mbar_init();
         prefetch_tmap(&tmX); prefetch_tmap(&tmB); prefetch_tmap(&tmC); prefetch_tmap(&tmY);
         sm->ticket = atomicAdd(a.ticket, 1);
@@ -406,6 +438,10 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     const int ticket = sm->ticket;
     const bool run = !status_bad(a.status);
 
+    // Roles.  Each role's code sits inside the branch that sets its register
+    // count, so that it is compiled for that count.
+    if (warp >= 8) {
+    if (warp < 12) regs_down<kRegProducer>(); else regs_down<kRegEpilogue>();
     if (warp == 8) {
         // ------------------------------------------------------------ TMA
         if (lane == 0 && run) {
@@ -417,10 +453,12 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 const int slot = k & 1;
                 {
                     // slot k % 4 last described block k - 4: the compute warps
-                    // were done with it (its epilogue included) before they
-                    // made block k - 2's H operand and Xw ready, which the
-                    // c_empty and b_empty completions waited for in the
-                    // previous iteration follow
+                    // were done with it before they made block k - 2's H
+                    // operand and Xw ready, which the c_empty and b_empty
+                    // completions waited for in the previous iteration
+                    // follow; the epilogue warps release it themselves
+                    if (!kPre && k >= kDescRing)
+                        fwait(&sm->desc_free[k % kDescRing], ((k / kDescRing) + 1) & 1, a.status);
                     BDesc &d = sm->desc[k % kDescRing];
                     const Lane &ln = w.ln;
                     const int i0 = w.b * kB;
@@ -566,14 +604,85 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                                smem_desc(sx + (uint32_t)(slot * HL + hh) * kT16 + kk * 2048, kT16,
                                          1024, kSwizzle128B),
                                id_mx, 1);
-                mma_commit(&sm->mx_done[slot]);
-                mma_commit(&sm->x_empty[slot]);
+                mma_commit(&sm->mx_done[slot]);   // (the epilogue frees the x slot)
             }
             // every MMA this thread issued has completed before TMEM is freed
             mma_commit(&sm->mma_fin);
             drain_wait(&sm->mma_fin, 0);
         }
-    } else if (run) {
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------ epilogue
+        // y of block k from the accumulator, off the compute warps' path.
+        // Thread t is TMEM lane t, i.e. token row t of the block.  The rows
+        // are staged, bf16 and swizzled, in the block's own x tiles: the M x
+        // product was their last reader, so they are free once it has
+        // landed, and they have y's shape and layout.  Thread 0 stores each
+        // head's tile with TMA and, once the store has read them, hands the
+        // x slot back to the TMA warp.  A block whose rows past the sequence
+        // belong to another packed sequence writes its rows one by one
+        // instead.
+        if (!kPre && run) {
+            const int t = tid & 127;
+            const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+            const uint32_t nblk = (uint32_t)cta_blocks(a, ticket);
+            for (uint32_t k = 0; k < nblk; ++k) {
+                const int slot = k & 1;
+                fwait(&sm->desc_full[k % kDescRing], (k / kDescRing) & 1, a.status);
+                const BDesc &dk = sm->desc[k % kDescRing];   // released after the store
+                const bool tma_y = (dk.flags & kTmaY) != 0;
+                fwait(&sm->mx_done[slot], (k >> 1) & 1, a.status);
+                tc_fence_after();
+                const uint32_t R_acc = tbase + 256 + Gm::ACC * slot;
+#pragma unroll 1
+                for (int hh = 0; hh < HL; ++hh) {
+                    uint4 *dst = tma_y
+                        ? (uint4 *)(sX + (size_t)(slot * HL + hh) * kT16 + t * 128)
+                        : (t < dk.rem && hh < dk.nh)
+                            ? (uint4 *)(a.y + (((int64_t)dk.row * a.L + dk.tok + t) * a.H + dk.h0 + hh) * kP)
+                            : nullptr;
+#pragma unroll 1
+                    for (int q = 0; q < 4; ++q) {   // 16 columns (two 16-byte chunks) at a time
+                        uint32_t v[16];
+                        tmem_ld16(R_acc + lane_off + hh * 64 + q * 16, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            const uint4 pk = make_uint4(
+                                pack_bf16x2(__uint_as_float(v[8 * c]), __uint_as_float(v[8 * c + 1])),
+                                pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3])),
+                                pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5])),
+                                pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])));
+                            // staged rows are swizzled like x (16-byte chunk j of
+                            // row t at chunk j ^ (t & 7)); direct rows are plain
+                            if (tma_y) dst[(2 * q + c) ^ (t & 7)] = pk;
+                            else if (dst) dst[2 * q + c] = pk;
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&sm->acc_free[slot]);
+                if (tma_y) fence_proxy_async_smem();
+                named_bar(4, 128);   // every row of the staged tiles is written
+                if (t == 0) {
+                    if (tma_y) {
+                        for (int hh = 0; hh < dk.nh; ++hh)
+                            tma_store_4d(&tmY, sX + (size_t)(slot * HL + hh) * kT16, 0, dk.h0 + hh,
+                                         dk.tok, dk.row);
+                        tma_store_commit();
+                    }
+                }
+                mbar_arrive(&sm->desc_free[k % kDescRing]);
+                if (t == 0) {
+                    if (tma_y) tma_store_wait_read0();
+                    mbar_arrive(&sm->x_empty[slot]);
+                }
+            }
+            if (t == 0) tma_store_wait0();
+        }
+    }
+    } else {
+    regs_up<kRegCompute>();
+    if (run) {
         // ------------------------------------------------------------ compute
         // Warpgroup h: thread t is TMEM lane t, i.e. token row i = t of the
         // block for C B^T, M and the outputs, and state row n = t for H.  For
@@ -606,7 +715,6 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             asm volatile("cp.async.commit_group;" ::: "memory");
         };
         bool have_next = false;
-        bool pend_store = false;   // a TMA store of y still reads this half of Xw
         float ldsum = 0.f;         // pre run: sum of cs_last over the lane's blocks here
         const uint32_t nblk = (uint32_t)cta_blocks(a, ticket);
 
@@ -728,13 +836,6 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 //     eight 16-byte chunks starting at a different one in each of
                 //     8 lanes
                 fwait(&sm->x_full[slot], (k >> 1) & 1, a.status);
-                if (t == 0 && pend_store) {
-                    tma_store_wait_read0();
-                    pend_store = false;
-                }
-                // the y store has read this half of Xw (wide: the one tile
-                // both warpgroups write, stored by thread 0)
-                if (kWide) named_bar(3, 256); else named_bar(bar_wg, 128);
                 {
                     const uint4 *src = (const uint4 *)(sX + (size_t)(slot * HL + hs) * kT16 + t * 128);
                     uint4 *dst = (uint4 *)(sXw + hs * kT16 + t * 128);
@@ -867,64 +968,6 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 fwait(&sm->s_done, k & 1, a.status);
                 tc_fence_after();
                 }
-            } else if (!kPre && k >= 1) {
-                // after the last block: the last y store has read its half of Xw
-                if (t == 0 && pend_store) tma_store_wait_read0();
-                if (kWide) named_bar(3, 256); else named_bar(bar_wg, 128);
-            }
-
-            // (c) epilogue of the previous block: acc (TMEM) -> bf16 -> this
-            //     head's half of Xw -> TMA store
-            if (!kPre && k >= 1) {
-                const uint32_t kk = k - 1;
-                const int ps = kk & 1;
-                fwait(&sm->mx_done[ps], (kk >> 1) & 1, a.status);
-                tc_fence_after();
-                const uint32_t R_prev = tbase + 256 + Gm::ACC * ps;
-                // how y leaves the chip: 0 no valid head here, 1 TMA store of
-                // the whole tile, 2 direct stores of the rows inside the sequence
-                const BDesc &dp = sm->desc[kk % kDescRing];
-                const bool hvp = hs < dp.nh;
-                const int prev_mode = !hvp ? 0 : (dp.flags & kTmaY) ? 1 : 2;
-                const int prev_head = dp.h0 + (hvp ? hs : 0);
-                const int64_t prev_y =
-                    (hvp && t < dp.rem) ? (((int64_t)dp.row * a.L + dp.tok + t) * a.H + prev_head) * kP : -1;
-                uint8_t *stile = sXw + (size_t)hs * kT16;
-                uint8_t *srow = stile + t * 128;
-                // narrow: head h's 64 columns in two halves; wide: half h of
-                // the one head's row
-#pragma unroll
-                for (int half = kWide ? h : 0; half < (kWide ? h + 1 : 2); ++half) {
-                    uint32_t v[32];
-                    tmem_ld32(R_prev + lane_off + (kWide ? 0 : h * 64) + half * 32, v);
-                    tmem_ld_wait();
-                    uint4 pk[4];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        pk[c] = make_uint4(
-                            pack_bf16x2(__uint_as_float(v[8 * c]), __uint_as_float(v[8 * c + 1])),
-                            pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3])),
-                            pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5])),
-                            pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])));
-                    if (prev_mode == 1) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            *(uint4 *)(srow + (((half * 4 + c) ^ (t & 7)) << 4)) = pk[c];
-                    } else if (prev_mode == 2 && prev_y >= 0) {
-                        uint4 *dst = (uint4 *)(a.y + prev_y + half * 32);
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) dst[c] = pk[c];
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(&sm->acc_free[ps]);
-                if (prev_mode == 1) fence_proxy_async_smem();
-                if (kWide) named_bar(3, 256); else named_bar(bar_wg, 128);
-                if (t == 0 && (!kWide || h == 0) && prev_mode == 1) {
-                    tma_store_4d(&tmY, stile, 0, prev_head, dp.tok, dp.row);
-                    tma_store_commit();
-                    pend_store = true;
-                }
             }
             if (!have) break;
 
@@ -967,7 +1010,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 }
             }
         }
-        if (t == 0) tma_store_wait0();
+    }
     }
     tc_fence_before();
     __syncthreads();
@@ -1171,6 +1214,17 @@ int fused_supported(const Problem &p) {
     return SSD_OK;
 }
 
+// The warpgroups trade registers (setmaxnreg); the trade adds up only with
+// the launch allocation it was sized for.  Any other allocation could leave
+// the increase waiting forever, so such a build is refused.
+template <typename K>
+cudaError_t check_regs(K kern) {
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    return fa.numRegs == kRegLaunch ? cudaSuccess : cudaErrorInvalidDeviceFunction;
+}
+
 cudaError_t fused_launch(const Problem &p) {
     const FLayout w = fused_layout(p);
     FArgs a{};
@@ -1225,6 +1279,8 @@ cudaError_t fused_launch(const Problem &p) {
         // pre run: the state records at every split; then the tickets start
         // again from zero for the main run
         Kern pre = pick(true);
+        e = check_regs(pre);
+        if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(pre, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         pre<<<w.grid, kThreads, smem, p.stream>>>(tmX, tmB, tmC, tmY, a);
@@ -1238,6 +1294,8 @@ cudaError_t fused_launch(const Problem &p) {
         a.chain = 1;
     }
     Kern kern = pick(false);
+    e = check_regs(kern);
+    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<w.grid, kThreads, smem, p.stream>>>(tmX, tmB, tmC, tmY, a);
