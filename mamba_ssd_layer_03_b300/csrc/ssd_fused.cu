@@ -964,9 +964,6 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 tc_fence_before();
                 mbar_arrive(&sm->m_ready);
 
-                // the S product of this block has read Xw once s_done completes
-                fwait(&sm->s_done, k & 1, a.status);
-                tc_fence_after();
                 }
             }
             if (!have) break;
@@ -979,7 +976,11 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 const int head = dk.h0 + (hv ? hs : 0);
                 const bool fin = (flags & kFin) != 0;
                 const int n_row = kWide ? 128 * h + t : t;   // this thread's state row
-                if (kPre) fwait(&sm->s_done, k & 1, a.status);   // (the main run waits below)
+                // S of this block has landed in H.  (This wait also covers the
+                // next block: a lane's first block here reloads H in TMEM and
+                // rewrites Xw, which S of this block reads.)
+                fwait(&sm->s_done, k & 1, a.status);
+                tc_fence_after();
                 float *dst = nullptr;
                 if (fin) {
                     // the pre run leaves final states to the main run
