@@ -730,6 +730,88 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 const uint32_t R_acc = tbase + 256 + Gm::ACC * slot;
                 const bool seg_start = (flags & kSegStart) != 0;
 
+                // (d) H_k -> H_op (bf16, operand of C H^T), then H <- decay H_k
+                //     in TMEM (after the scan), ready for the S product to
+                //     accumulate on.  A lane's first block takes H_k from the
+                //     initial state (or the previous CTA's handoff) through TMEM.
+                //     Narrow lanes do the first part before the scan, so that
+                //     C H^T runs while the scan does; wide lanes after it (their
+                //     S product of the previous block, which H_k waits for, and
+                //     their larger C H^T are better left behind the scan:
+                //     measured).
+                auto state_in = [&]() {
+                    if (seg_start) {
+                        // A lane split at this CTA's range start begins from: zero
+                        // (pre run); the fold of the earlier CTAs' pre-run records
+                        // (main run of a few-lane workload); or the previous CTA's
+                        // handoff.
+                        const float *src = nullptr;
+                        const int n_row = kWide ? 128 * h + t : t;   // this thread's state row
+                        if (flags & kFromSlot) {
+                            if (kPre) {
+                            } else if (a.chain) {
+                                // folded from the pre run's records between the runs
+                                src = a.hstart + (size_t)ticket * kStateFloats + hs * kP * NS;
+                            } else {
+                                wait_flag(a.hflag + (ticket - 1), a.status);
+                                src = a.hslot + (size_t)(ticket - 1) * kStateFloats + hs * kP * NS;
+                            }
+                        } else if (a.init && hv) {
+                            src = a.init + ((int64_t)dk.s * a.H + head) * kP * NS;
+                        }
+                        if (!hv) src = nullptr;
+                        // 16 loads in flight per round: the state's 64 columns
+                        // arrive in a few memory latencies, not sixteen
+                        if (src) {
+                            for (int c16 = 0; c16 < kP / 16; ++c16) {
+                                uint32_t r[16];
+#pragma unroll
+                                for (int q = 0; q < 16; ++q)
+                                    r[q] = __float_as_uint(__ldcg(src + (c16 * 16 + q) * NS + n_row));
+                                tmem_st16(R_H + lane_off + h * 64 + c16 * 16, r);
+                            }
+                        } else {
+                            uint32_t r[16];
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) r[q] = 0u;
+#pragma unroll 1
+                            for (int c16 = 0; c16 < kP / 16; ++c16) tmem_st16(R_H + lane_off + h * 64 + c16 * 16, r);
+                        }
+                        tmem_st_wait();
+                    } else {
+                        fwait(&sm->s_done, (k - 1) & 1, a.status);
+                        tc_fence_after();
+                    }
+                };
+                // H_k of this thread's state row -> H_op, then C H^T may
+                // start.  Narrow lanes publish it before the scan and keep H_k
+                // in registers over it; wide lanes, whose C H^T reads twice the
+                // operands, after it (measured: the early product slows their
+                // scan more than it gains).
+                uint32_t hv2[2][32];
+                auto publish_hop = [&]() {
+                    tmem_ld32(R_H + lane_off + h * 64, hv2[0]);
+                    tmem_ld32(R_H + lane_off + h * 64 + 32, hv2[1]);
+                    tmem_ld_wait();
+                    uint8_t *hrow = sH + h * kT16 + t * 128;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            if (!kPre) *(uint4 *)(hrow + (((half * 4 + c) ^ (t & 7)) << 4)) = make_uint4(
+                                pack_bf16x2(__uint_as_float(hv2[half][8 * c]), __uint_as_float(hv2[half][8 * c + 1])),
+                                pack_bf16x2(__uint_as_float(hv2[half][8 * c + 2]), __uint_as_float(hv2[half][8 * c + 3])),
+                                pack_bf16x2(__uint_as_float(hv2[half][8 * c + 4]), __uint_as_float(hv2[half][8 * c + 5])),
+                                pack_bf16x2(__uint_as_float(hv2[half][8 * c + 6]), __uint_as_float(hv2[half][8 * c + 7])));
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&sm->hop_ready);
+                };
+                if (!kWide) {
+                    state_in();
+                    publish_hop();
+                }
+
                 // (a) dt and the within-block cumulative decay cs of head h
                 if (!have_next) prefetch_dt(dk, 0, slot);
                 asm volatile("cp.async.wait_all;" ::: "memory");
@@ -758,77 +840,19 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 }
                 const float w_t = __expf(fminf(cs_last - incl, 0.f)) * d;
                 const float decay = __expf(cs_last);
+                if (kWide) {
+                    state_in();
+                    publish_hop();
+                }
 
-                // (d) H_k -> H_op (bf16, operand of C H^T) and H <- decay H_k in
-                //     TMEM, ready for the S product to accumulate on.  A lane's
-                //     first block takes H_k from the initial state (or the
-                //     previous CTA's handoff) through TMEM.
                 if (kPre && seg_start) ldsum = 0.f;
                 if (kPre) ldsum += cs_last;
-                if (seg_start) {
-                    // A lane split at this CTA's range start begins from: zero
-                    // (pre run); the fold of the earlier CTAs' pre-run records
-                    // (main run of a few-lane workload); or the previous CTA's
-                    // handoff.
-                    const float *src = nullptr;
-                    const int n_row = kWide ? 128 * h + t : t;   // this thread's state row
-                    if (flags & kFromSlot) {
-                        if (kPre) {
-                        } else if (a.chain) {
-                            // folded from the pre run's records between the runs
-                            src = a.hstart + (size_t)ticket * kStateFloats + hs * kP * NS;
-                        } else {
-                            wait_flag(a.hflag + (ticket - 1), a.status);
-                            src = a.hslot + (size_t)(ticket - 1) * kStateFloats + hs * kP * NS;
-                        }
-                    } else if (a.init && hv) {
-                        src = a.init + ((int64_t)dk.s * a.H + head) * kP * NS;
-                    }
-                    if (!hv) src = nullptr;
-                    // 16 loads in flight per round: the state's 64 columns
-                    // arrive in a few memory latencies, not sixteen
-                    if (src) {
-                        for (int c16 = 0; c16 < kP / 16; ++c16) {
-                            uint32_t r[16];
 #pragma unroll
-                            for (int q = 0; q < 16; ++q)
-                                r[q] = __float_as_uint(__ldcg(src + (c16 * 16 + q) * NS + n_row));
-                            tmem_st16(R_H + lane_off + h * 64 + c16 * 16, r);
-                        }
-                    } else {
-                        uint32_t r[16];
+                for (int half = 0; half < 2; ++half) {
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) r[q] = 0u;
-#pragma unroll 1
-                        for (int c16 = 0; c16 < kP / 16; ++c16) tmem_st16(R_H + lane_off + h * 64 + c16 * 16, r);
-                    }
-                    tmem_st_wait();
-                } else {
-                    fwait(&sm->s_done, (k - 1) & 1, a.status);
-                    tc_fence_after();
+                    for (int q = 0; q < 32; q += 2) mul2(hv2[half][q], hv2[half][q + 1], decay, decay);
+                    tmem_st32(R_H + lane_off + h * 64 + half * 32, hv2[half]);
                 }
-                {
-                    uint8_t *hrow = sH + h * kT16 + t * 128;
-                    uint32_t v[2][32];
-                    tmem_ld32(R_H + lane_off + h * 64, v[0]);
-                    tmem_ld32(R_H + lane_off + h * 64 + 32, v[1]);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            if (!kPre) *(uint4 *)(hrow + (((half * 4 + c) ^ (t & 7)) << 4)) = make_uint4(
-                                pack_bf16x2(__uint_as_float(v[half][8 * c]), __uint_as_float(v[half][8 * c + 1])),
-                                pack_bf16x2(__uint_as_float(v[half][8 * c + 2]), __uint_as_float(v[half][8 * c + 3])),
-                                pack_bf16x2(__uint_as_float(v[half][8 * c + 4]), __uint_as_float(v[half][8 * c + 5])),
-                                pack_bf16x2(__uint_as_float(v[half][8 * c + 6]), __uint_as_float(v[half][8 * c + 7])));
-#pragma unroll
-                        for (int q = 0; q < 32; q += 2) mul2(v[half][q], v[half][q + 1], decay, decay);
-                        tmem_st32(R_H + lane_off + h * 64 + half * 32, v[half]);
-                    }
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&sm->hop_ready);
 
                 // (b) Xw_h row t = w_t x_h row t, one packed bf16 x bf16 multiply
                 //     per pair (w_t rounded to bf16 first: relative error 2^-8 on
