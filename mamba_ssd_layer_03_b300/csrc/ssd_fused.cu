@@ -303,6 +303,20 @@ __device__ __forceinline__ void regs_down() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Programmatic dependent launch.  A split call's three kernels are launched
+// so that the next one may start while the previous one finishes:
+// launch_dependents lets the next grid be scheduled once every CTA of this
+// one has issued it, and wait blocks until every grid this one depends on
+// has completed and its memory operations are visible (it returns at once
+// for a grid launched the ordinary way).  The earlier grids always finish
+// (every wait in them is bounded), so neither can wait forever.
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Plain bounded wait used only while draining at exit.
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
@@ -428,6 +442,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         fence_mbar_init();
         prefetch_tmap(&tmX); prefetch_tmap(&tmB); prefetch_tmap(&tmC); prefetch_tmap(&tmY);
         sm->ticket = atomicAdd(a.ticket, 1);
+        grid_dep_launch();
     }
     if (warp == 0) { tmem_alloc(&sm->tmem, 512); tmem_relinquish(); }
     tc_fence_before();
@@ -717,6 +732,9 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         bool have_next = false;
         float ldsum = 0.f;         // pre run: sum of cs_last over the lane's blocks here
         const uint32_t nblk = (uint32_t)cta_blocks(a, ticket);
+        // the main run of a split call starts splits from the fold's states:
+        // wait for the fold (and with it the pre run) to complete
+        grid_dep_wait();
 
         for (uint32_t k = 0;; ++k) {
             const bool have = k < nblk;
@@ -1054,6 +1072,8 @@ constexpr int kFoldThreads = 256;
 constexpr int kFoldSlices = kStateFloats / (4 * kFoldThreads);
 static_assert(kStateFloats % (4 * kFoldThreads) == 0, "fold slices");
 __global__ void __launch_bounds__(kFoldThreads) k_fused_chain_fold(FArgs a, int NS) {
+    if (threadIdx.x == 0) grid_dep_launch();
+    grid_dep_wait();   // the pre run's records
     if (status_bad(a.status)) return;
     const int ticket = blockIdx.y;
     const int64_t T = total_blocks(a);
@@ -1242,6 +1262,25 @@ int fused_supported(const Problem &p) {
 // The warpgroups trade registers (setmaxnreg); the trade adds up only with
 // the launch allocation it was sized for.  Any other allocation could leave
 // the increase waiting forever, so such a build is refused.
+// A launch that may overlap the previous kernel on the stream (programmatic
+// stream serialization); the kernel waits with griddepcontrol.wait before it
+// reads what the previous kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, int threads, size_t smem,
+                             cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <typename K>
 cudaError_t check_regs(K kern) {
     cudaFuncAttributes fa;
@@ -1311,11 +1350,12 @@ cudaError_t fused_launch(const Problem &p) {
         pre<<<w.grid, kThreads, smem, p.stream>>>(tmX, tmB, tmC, tmY, a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        k_fused_chain_fold<<<dim3(kFoldSlices, w.grid), kFoldThreads, 0, p.stream>>>(a, p.N);
-        e = cudaGetLastError();
+        e = launch_dependent(k_fused_chain_fold, dim3(kFoldSlices, w.grid), kFoldThreads, 0, p.stream,
+                             a, p.N);
         if (e != cudaSuccess) return e;
-        e = cudaMemsetAsync(p.ws + w.hdr, 0, w.slots - w.hdr, p.stream);
-        if (e != cudaSuccess) return e;
+        // the main run draws its tickets from a second counter (zeroed with
+        // the first), so that no memset separates the kernels
+        a.ticket += 1;
         a.chain = 1;
     }
     Kern kern = pick(false);
@@ -1323,6 +1363,8 @@ cudaError_t fused_launch(const Problem &p) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    if (w.chain)
+        return launch_dependent(kern, dim3(w.grid), kThreads, smem, p.stream, tmX, tmB, tmC, tmY, a);
     kern<<<w.grid, kThreads, smem, p.stream>>>(tmX, tmB, tmC, tmY, a);
     return cudaGetLastError();
 }
