@@ -451,6 +451,9 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     const uint32_t tbase = sm->tmem;
     const uint32_t R_cb = tbase, R_H = tbase + 128;
     const int ticket = sm->ticket;
+    // packed sequences: every role reads the lane table that
+    // k_fused_varlen_setup, launched just before, writes
+    if (a.varlen) grid_dep_wait();
     const bool run = !status_bad(a.status);
 
     // Roles.  Each role's code sits inside the branch that sets its register
@@ -1100,6 +1103,7 @@ __global__ void __launch_bounds__(kFoldThreads) k_fused_chain_fold(FArgs a, int 
 // Varlen set-up: blocks per sequence (exclusive prefix) and the final states
 // of empty sequences (their initial states).  One CTA.
 __global__ void k_fused_varlen_setup(FArgs a, int P, int N) {
+    if (threadIdx.x == 0) grid_dep_launch();   // the scan may be scheduled; it waits for this
     if (status_bad(a.status)) return;
     __shared__ int carry;
     __shared__ int warp_sum[32];
@@ -1347,8 +1351,12 @@ cudaError_t fused_launch(const Problem &p) {
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(pre, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        pre<<<w.grid, kThreads, smem, p.stream>>>(tmX, tmB, tmC, tmY, a);
-        e = cudaGetLastError();
+        if (a.varlen) {
+            e = launch_dependent(pre, dim3(w.grid), kThreads, smem, p.stream, tmX, tmB, tmC, tmY, a);
+        } else {
+            pre<<<w.grid, kThreads, smem, p.stream>>>(tmX, tmB, tmC, tmY, a);
+            e = cudaGetLastError();
+        }
         if (e != cudaSuccess) return e;
         e = launch_dependent(k_fused_chain_fold, dim3(kFoldSlices, w.grid), kFoldThreads, 0, p.stream,
                              a, p.N);
@@ -1363,7 +1371,7 @@ cudaError_t fused_launch(const Problem &p) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    if (w.chain)
+    if (w.chain || a.varlen)
         return launch_dependent(kern, dim3(w.grid), kThreads, smem, p.stream, tmX, tmB, tmC, tmY, a);
     kern<<<w.grid, kThreads, smem, p.stream>>>(tmX, tmB, tmC, tmY, a);
     return cudaGetLastError();
