@@ -113,11 +113,21 @@ __global__ void __launch_bounds__(kK1Threads) k1_chunk_cumsum(KArgs a) {
     }
 }
 
-// K2: grid (nc, batch, H), block 256; threads over (p, n).
+// K2: grid (nc, batch, H), block 256; threads over (p, n).  The chunk's
+// weighted x (w_j x_j, head h) and B (group g) are staged in shared memory
+// k2_tile() tokens at a time with coalesced loads, all in flight at once, so
+// that the token loop reads shared memory instead of waiting on one cache
+// line per token.
+__host__ __device__ inline int k2_tile(int P, int N) { return P + N <= 256 ? 32 : 16; }
+
 template <typename T>
 __global__ void k2_chunk_state(KArgs a) {
     if (status_bad(a.status)) return;
-    extern __shared__ float w_smem[];  // [Q] weights exp(cs_last - cs_j) dt_j
+    extern __shared__ float k2s[];   // w[Q], xs[tile][P], bs[tile][N]
+    const int TJ = k2_tile(a.P, a.N);
+    float *w_smem = k2s;
+    float *xs = k2s + a.Q;
+    float *bs = xs + TJ * a.P;
     const int c = blockIdx.x, r = blockIdx.y, h = blockIdx.z;
     const int g = h / a.hpg;
     const int64_t t0 = (int64_t)c * a.Q;
@@ -132,20 +142,35 @@ __global__ void k2_chunk_state(KArgs a) {
             w = (float)exp(cl - cs[j]) * __ldg(a.dt + ((int64_t)r * a.L + t0 + j) * a.H + h);
         w_smem[j] = w;
     }
-    __syncthreads();
     const T *x = (const T *)a.x;
     const T *B = (const T *)a.B;
     const int PN = a.P * a.N;
     float *S = a.S + st_index(a, r, c, h);
-    for (int e = threadIdx.x; e < PN; e += blockDim.x) {
+    for (int e0 = 0; e0 < PN; e0 += blockDim.x) {
+        const int e = e0 + threadIdx.x;
         const int p = e / a.N, n = e % a.N;
         float acc = 0.f;
-        for (int j = j0; j < len; ++j) {
-            const int64_t tok = (int64_t)r * a.L + t0 + j;
-            acc += w_smem[j] * ld_as_float(x + (tok * a.H + h) * a.P + p) *
-                   ld_as_float(B + (tok * a.G + g) * a.N + n);
+        for (int jt = j0; jt < len; jt += TJ) {
+            const int nj = min(TJ, len - jt);
+            __syncthreads();   // the weights are written; the previous tile is used up
+            // unrolled: several loads in flight before their stores
+#pragma unroll 4
+            for (int idx = threadIdx.x; idx < nj * a.P; idx += blockDim.x) {
+                const int jj = idx / a.P, pp = idx % a.P;
+                const int64_t tok = (int64_t)r * a.L + t0 + jt + jj;
+                xs[jj * a.P + pp] = w_smem[jt + jj] * ld_as_float(x + (tok * a.H + h) * a.P + pp);
+            }
+#pragma unroll 4
+            for (int idx = threadIdx.x; idx < nj * a.N; idx += blockDim.x) {
+                const int jj = idx / a.N, nn = idx % a.N;
+                const int64_t tok = (int64_t)r * a.L + t0 + jt + jj;
+                bs[jj * a.N + nn] = ld_as_float(B + (tok * a.G + g) * a.N + nn);
+            }
+            __syncthreads();
+            if (e < PN)
+                for (int jj = 0; jj < nj; ++jj) acc += xs[jj * a.P + p] * bs[jj * a.N + n];
         }
-        S[e] = acc;
+        if (e < PN) S[e] = acc;
     }
 }
 
@@ -268,10 +293,21 @@ __global__ void k5_seq_final(KArgs a) {
 constexpr int kPT = 16;  // output columns (p) per thread in K4
 
 // K4: grid (nc, batch, H * ceil(P/16)), block Q; thread i owns token i of
-// the chunk and 16 consecutive p columns.
+// the chunk and 16 consecutive p columns.  B (group g), the 16 x columns,
+// dt and cs of the chunk are staged in shared memory kK4Tile tokens at a
+// time with coalesced loads, and the entry state's 16 rows after them, so
+// that the token loop reads shared memory.
+constexpr int kK4Tile = 32;
+constexpr int kCiRegs = 32;   // dstate up to which C_i is held in registers
+
 template <typename T>
 __global__ void k4_chunk_output(KArgs a) {
     if (status_bad(a.status)) return;
+    extern __shared__ float k4s[];   // bs[tile][N] (later E rows [16][N]), xs[tile][16], dts[tile], csj[tile] (double)
+    float *bs = k4s;
+    float *xs = bs + kK4Tile * a.N;   // (kK4Tile >= 16: the E rows fit where B was)
+    float *dts = xs + kK4Tile * kPT;
+    double *csj = (double *)(dts + kK4Tile);
     const int c = blockIdx.x, r = blockIdx.y;
     const int npt = (a.P + kPT - 1) / kPT;
     const int h = blockIdx.z / npt, p0 = (blockIdx.z % npt) * kPT;
@@ -279,14 +315,14 @@ __global__ void k4_chunk_output(KArgs a) {
     const int64_t t0 = (int64_t)c * a.Q;
     const int len = (int)min64(a.Q, a.L - t0);
     const int i = threadIdx.x;
-    if (i >= len) return;
-    const int64_t ti = t0 + i;
+    const bool active = i < len;
+    const int64_t ti = t0 + min(i, len - 1);
     const int64_t tok_i = (int64_t)r * a.L + ti;
     const int si = seq_of(a, r, ti);
     const int fs = seq_of(a, r, t0);
     const int j0 = (int)max64(0, seq_start(a, si) - t0);
     const double *cs = a.cs + cs_index(a, r, h, c);
-    const double csi = cs[i];
+    const double csi = cs[min(i, len - 1)];
     const T *x = (const T *)a.x;
     const T *B = (const T *)a.B;
     const T *C = (const T *)a.C;
@@ -294,28 +330,82 @@ __global__ void k4_chunk_output(KArgs a) {
     float acc[kPT];
 #pragma unroll
     for (int q = 0; q < kPT; ++q) acc[q] = 0.f;
-    for (int j = j0; j <= i; ++j) {
-        const int64_t tok_j = (int64_t)r * a.L + t0 + j;
-        const T *Bj = B + (tok_j * a.G + g) * a.N;
-        float cb = 0.f;
-        for (int n = 0; n < a.N; ++n) cb += ld_as_float(Ci + n) * ld_as_float(Bj + n);
-        const float w = cb * expf((float)(csi - cs[j])) * __ldg(a.dt + tok_j * a.H + h);
-        const T *xj = x + (tok_j * a.H + h) * a.P;
+    // C_i in registers when the state is small (the token loop's dot
+    // products then wait on nothing but shared memory)
+    float ci[kCiRegs];
 #pragma unroll
-        for (int q = 0; q < kPT; ++q)
-            if (p0 + q < a.P) acc[q] += w * ld_as_float(xj + p0 + q);
+    for (int n = 0; n < kCiRegs; ++n) ci[n] = (n < a.N) ? ld_as_float(Ci + n) : 0.f;
+    for (int jt = 0; jt < len; jt += kK4Tile) {   // the same trip count in every thread
+        const int nj = min(kK4Tile, len - jt);
+        __syncthreads();
+        // unrolled: several loads in flight before their stores
+#pragma unroll 4
+        for (int idx = threadIdx.x; idx < nj * a.N; idx += blockDim.x) {
+            const int jj = idx / a.N, nn = idx % a.N;
+            const int64_t tok = (int64_t)r * a.L + t0 + jt + jj;
+            bs[jj * a.N + nn] = ld_as_float(B + (tok * a.G + g) * a.N + nn);
+        }
+#pragma unroll 4
+        for (int idx = threadIdx.x; idx < nj * kPT; idx += blockDim.x) {
+            const int jj = idx / kPT, q = idx % kPT;
+            const int64_t tok = (int64_t)r * a.L + t0 + jt + jj;
+            xs[jj * kPT + q] = (p0 + q < a.P) ? ld_as_float(x + (tok * a.H + h) * a.P + p0 + q) : 0.f;
+        }
+        for (int jj = threadIdx.x; jj < nj; jj += blockDim.x) {
+            const int64_t tok = (int64_t)r * a.L + t0 + jt + jj;
+            dts[jj] = __ldg(a.dt + tok * a.H + h);
+            csj[jj] = cs[jt + jj];
+        }
+        __syncthreads();
+        if (active) {
+            const int jb = max(j0, jt), je = min(i, jt + nj - 1);
+            for (int j = jb; j <= je; ++j) {
+                const int jj = j - jt;
+                const float *Bj = bs + jj * a.N;
+                float cb = 0.f;
+                if (a.N <= kCiRegs) {
+#pragma unroll
+                    for (int n = 0; n < kCiRegs; ++n)
+                        if (n < a.N) cb += ci[n] * Bj[n];
+                } else {
+                    for (int n = 0; n < a.N; ++n) cb += ld_as_float(Ci + n) * Bj[n];
+                }
+                const float w = cb * expf((float)(csi - csj[jj])) * dts[jj];
+#pragma unroll
+                for (int q = 0; q < kPT; ++q) acc[q] += w * xs[jj * kPT + q];
+            }
+        }
     }
     const int PN = a.P * a.N;
     const float *E = (si == fs) ? a.E + st_index(a, r, c, h)
                                 : (a.init ? a.init + ((int64_t)si * a.H + h) * PN : nullptr);
+    // E rows p0 .. p0 + 15 (every thread of the chunk reads the same ones
+    // unless a packed sequence starts inside the chunk): staged when shared
+    const bool shared_E = (a.varlen == false);
+    if (shared_E) {
+        __syncthreads();
+        if (E)
+            for (int idx = threadIdx.x; idx < kPT * a.N; idx += blockDim.x) {
+                const int q = idx / a.N;
+                bs[idx] = (p0 + q < a.P) ? E[(int64_t)(p0 + q) * a.N + idx % a.N] : 0.f;
+            }
+        __syncthreads();
+    }
+    if (!active) return;
     if (E) {
         const float dec = expf((float)csi);
 #pragma unroll
         for (int q = 0; q < kPT; ++q) {
             if (p0 + q >= a.P) continue;
-            const float *Ep = E + (int64_t)(p0 + q) * a.N;
+            const float *Ep = shared_E ? bs + q * a.N : E + (int64_t)(p0 + q) * a.N;
             float s = 0.f;
-            for (int n = 0; n < a.N; ++n) s += ld_as_float(Ci + n) * Ep[n];
+            if (a.N <= kCiRegs) {
+#pragma unroll
+                for (int n = 0; n < kCiRegs; ++n)
+                    if (n < a.N) s += ci[n] * Ep[n];
+            } else {
+                for (int n = 0; n < a.N; ++n) s += ld_as_float(Ci + n) * Ep[n];
+            }
             acc[q] += dec * s;
         }
     }
@@ -325,6 +415,11 @@ __global__ void k4_chunk_output(KArgs a) {
 #pragma unroll
     for (int q = 0; q < kPT; ++q)
         if (p0 + q < a.P) st_from_float(y + p0 + q, acc[q] + Dh * ld_as_float(xi + p0 + q));
+}
+
+static_assert(kK4Tile >= kPT, "the entry state's rows reuse the B tile");
+size_t k4_smem_bytes(int N) {
+    return (size_t)(kK4Tile * N + kK4Tile * kPT + kK4Tile) * sizeof(float) + kK4Tile * sizeof(double);
 }
 
 struct WsLayout {
@@ -356,13 +451,14 @@ cudaError_t launch_all(const Problem &p) {
     a.E = (float *)(p.ws + w.E);
     const unsigned b = (unsigned)p.batch;
     k1_chunk_cumsum<<<dim3(p.nc, b, (p.H + 31) / 32), kK1Threads, 0, p.stream>>>(a);
-    k2_chunk_state<T><<<dim3(p.nc, b, p.H), 256, p.Q * sizeof(float), p.stream>>>(a);
+    const size_t k2_smem = (size_t)(p.Q + k2_tile(p.P, p.N) * (p.P + p.N)) * sizeof(float);
+    k2_chunk_state<T><<<dim3(p.nc, b, p.H), 256, k2_smem, p.stream>>>(a);
     const int PN = p.P * p.N;
     k3_state_passing<<<dim3((PN + 255) / 256, p.H, b), 256, 0, p.stream>>>(a);
     if (a.varlen && p.final_states)
         k5_seq_final<T><<<dim3(p.nseq, p.H), 256, p.Q * sizeof(float), p.stream>>>(a);
     const int npt = (p.P + kPT - 1) / kPT;
-    k4_chunk_output<T><<<dim3(p.nc, b, p.H * npt), p.Q, 0, p.stream>>>(a);
+    k4_chunk_output<T><<<dim3(p.nc, b, p.H * npt), p.Q, k4_smem_bytes(p.N), p.stream>>>(a);
     return cudaGetLastError();
 }
 
