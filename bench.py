@@ -647,9 +647,9 @@ def run_step_bench(args, w, rank, world, local):
 def run_seqpar_bench(args, w, rank, world, local):
     """Device work of one rank of the sequence-parallel scan (seqpar.py): the
     last of ``--shards`` consecutive shards of every sequence of workload w,
-    which folds the most carries.  A step is the scan of the shard from a
-    zero state, its log-decay, the fold of all shards' carries into its entry
-    state and the final state, and the re-scan from the entry state.  The
+    which folds the most carries.  A step is the shard's state-only scan from
+    a zero state, its log-decay, the fold of all shards' carries into its
+    entry state and the final state, and the scan from the entry state.  The
     all_gather is not in the step (one GPU: there is no peer); the other
     shards' carries are stand-ins of the right size, and the rank's own carry
     is copied into its slot as the collective would place it."""
@@ -674,7 +674,7 @@ def run_seqpar_bench(args, w, rank, world, local):
                                      .multi_processor_count) + 2
 
     def step():
-        _, S = ops.scan(d["x"], d["dt"], d["A"], d["B"], d["C"], None, inp["chunk"], None, out=y)
+        S = ops.states(d["x"], d["dt"], d["A"], d["B"], d["C"], inp["chunk"])
         ld = ops.logdec(d["dt"], d["A"])
         S_all[me].copy_(S)
         ld_all[me].copy_(ld)
@@ -711,10 +711,12 @@ def run_seqpar_bench(args, w, rank, world, local):
     ms = ev0.elapsed_time(ev1) / args.steps
     scan_bytes, _, _ = workload_cost(inp)
     state = b * H * P * N * 4
-    # two scans (the first without D and initial states), the log-decay's dt
-    # read, the fold's R carries read, initial states read, entry and final
-    # states written
-    nbytes = 2 * scan_bytes + b * Ls * H * 4 + R * (state + b * H * 4) + 3 * state
+    # the state-only scan (x, B, dt read, states written), the full scan, the
+    # log-decay's dt read, the fold's R carries read, initial states read,
+    # entry and final states written
+    esz = 2 if inp["dtype"] == "bf16" else 4
+    first = b * Ls * (H * P * esz + inp["ngroups"] * N * esz + H * 4) + state
+    nbytes = first + scan_bytes + b * Ls * H * 4 + R * (state + b * H * 4) + 3 * state
     peaks = load_peaks()
     if rank == 0:
         out = {

@@ -189,6 +189,31 @@ SSD_API int ssd_scan_ex(const ssd_shape *shape, const void *x, const float *dt,
                         size_t workspace_bytes, void *stream);
 
 /*
+ * Final states only: what ssd_scan_ex() writes to final_states, without y
+ * (the state recurrence of the operation above, with no output read-out:
+ * no C, no D, no y).  For callers that need only where a sequence ends, for
+ * example the first pass of the sequence-parallel scan below, where each
+ * shard's end state from a zero start is all the exchange needs.  It runs
+ * the fused kernel's state-only mode, which skips C B^T, C H^T, the mask and
+ * M x, so it reads x, B and dt once and writes only the states.
+ *   shape          as for ssd_scan(); algo must be SSD_ALGO_AUTO or
+ *                  SSD_ALGO_TC and the shape one the fused kernel takes (bf16,
+ *                  headdim 64, dstate 128 or 256), else SSD_ERR_UNSUPPORTED
+ *   x, dt, A, B    required (layouts above); dt_transform nullable
+ *   initial_states nullable (zero); cu_seqlens nullable (as for ssd_scan())
+ *   final_states   required output, [nseq][nheads][headdim][dstate] fp32
+ *   workspace      >= ssd_scan_ex_workspace_size() of the same shape and
+ *                  transform, 256-byte aligned
+ * x, B, initial_states and final_states 16-byte aligned.  Errors and the
+ * device status word as for ssd_scan(); asynchronous on `stream`.
+ */
+SSD_API int ssd_scan_states(const ssd_shape *shape, const void *x, const float *dt,
+                            const ssd_dt_transform *dt_transform, const float *A,
+                            const void *B, const float *initial_states,
+                            const int32_t *cu_seqlens, float *final_states, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/*
  * One decode step of `batch` independent sequences: the recurrent form of the
  * same map, one token per sequence, with the state updated in place (the
  * selective SSM's state cache that makes generation linear-time: Mamba-1

@@ -103,6 +103,8 @@ def load_library() -> ctypes.CDLL:
     lib.ssd_scan_ex_workspace_size.restype = ctypes.c_int
     lib.ssd_scan_ex.argtypes = [sp, vp, vp, tp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.ssd_scan_ex.restype = ctypes.c_int
+    lib.ssd_scan_states.argtypes = [sp, vp, vp, tp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.ssd_scan_states.restype = ctypes.c_int
     lib.ssd_step.argtypes = [ctypes.POINTER(SsdStepShape), vp, vp, tp, vp, vp, vp, vp, vp, vp, vp]
     lib.ssd_step.restype = ctypes.c_int
     lib.ssd_selftest_wait_timeout.argtypes = [ctypes.c_int, vp, vp]
@@ -257,6 +259,66 @@ def ssd_scan(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor
         if rc != 0:
             raise SsdError(rc, "ssd_scan (device)")
     return y, fin
+
+
+def ssd_scan_states(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                    chunk_size: int = 256, initial_states: Optional[torch.Tensor] = None,
+                    cu_seqlens: Optional[torch.Tensor] = None, algo: str = "auto",
+                    final_out: Optional[torch.Tensor] = None,
+                    workspace: Optional[torch.Tensor] = None, check_status: bool = False,
+                    dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = False,
+                    dt_limit=None) -> torch.Tensor:
+    """Final states only (``ssd_scan_states``): what ``ssd_scan`` returns as
+    final_states, without computing y.  CUDA tensors; the shape must be one
+    the fused tensor-core kernel takes (bf16, headdim 64, dstate 128 or 256),
+    else SsdError(SSD_ERR_UNSUPPORTED).  Returns (nseq, H, P, N) fp32."""
+    lib = load_library()
+    if not isinstance(x, torch.Tensor) or x.dim() != 4:
+        raise ValueError("x must be a (batch, seqlen, nheads, headdim) tensor")
+    if not isinstance(B, torch.Tensor) or B.dim() != 4:
+        raise ValueError("B must be a (batch, seqlen, ngroups, dstate) tensor")
+    dev = x.device
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    _check(x, "x", x.dtype, device=dev)
+    _check(dt, "dt", torch.float32, (b, L, H), dev)
+    _check(A, "A", torch.float32, (H,), dev)
+    _check(B, "B", x.dtype, (b, L, G, N), dev)
+    nseq = b
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, device=dev)
+        nseq = cu_seqlens.numel() - 1
+    if initial_states is not None:
+        _check(initial_states, "initial_states", torch.float32, (nseq, H, P, N), dev)
+    if dt_bias is not None:
+        _check(dt_bias, "dt_bias", torch.float32, (H,), dev)
+    if final_out is not None:
+        _check(final_out, "final_out", torch.float32, (nseq, H, P, N), dev)
+    if workspace is not None:
+        _check(workspace, "workspace", torch.uint8, device=dev)
+    if dev.type != "cuda":
+        raise ValueError("ssd_scan_states runs on CUDA tensors")
+    tf = make_dt_transform(dt_bias, dt_softplus, dt_limit)
+    shape = make_shape(b, L, H, P, N, G, chunk_size, nseq, x.dtype, algo)
+    nbytes = workspace_size(shape, tf)
+    with torch.cuda.device(dev):
+        if workspace is None or workspace.numel() < nbytes:
+            workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        fin = final_out if final_out is not None else torch.empty(
+            (nseq, H, P, N), dtype=torch.float32, device=dev)
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        rc = lib.ssd_scan_states(ctypes.byref(shape), _ptr(x), _ptr(dt),
+                                 None if tf is None else ctypes.byref(tf), _ptr(A), _ptr(B),
+                                 _ptr(initial_states), _ptr(cu_seqlens), _ptr(fin),
+                                 _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                                 ctypes.c_void_p(stream))
+        if rc != 0:
+            raise SsdError(rc, "ssd_scan_states")
+        if check_status:
+            rc = lib.ssd_check_device_status(_ptr(workspace), ctypes.c_void_p(stream))
+            if rc != 0:
+                raise SsdError(rc, "ssd_scan_states (device)")
+    return fin
 
 
 def ssd_scan_noalloc(x, dt, A, B, C, D=None, chunk_size=256, initial_states=None,

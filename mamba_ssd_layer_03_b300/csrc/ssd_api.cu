@@ -252,6 +252,54 @@ SSD_API int ssd_step(const ssd_step_shape *shape, const void *x, const float *dt
     return step_launch(p) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
+SSD_API int ssd_scan_states(const ssd_shape *shape, const void *x, const float *dt,
+                            const ssd_dt_transform *dt_transform, const float *A, const void *B,
+                            const float *initial_states, const int32_t *cu_seqlens,
+                            float *final_states, void *workspace, size_t workspace_bytes,
+                            void *stream) {
+    Problem p;
+    int algo = 0;
+    int rc = resolve(shape, p, &algo);
+    if (rc != SSD_OK) return rc;
+    if (algo != SSD_ALGO_TC) return SSD_ERR_UNSUPPORTED;   // the fused kernel's shapes only
+    rc = resolve_dtt(dt_transform, p.dtt);
+    if (rc != SSD_OK) return rc;
+    if (cu_seqlens) {
+        if (p.batch != 1 || p.nseq < 1) return SSD_ERR_INVALID_ARG;
+    } else if (p.nseq != p.batch) {
+        return SSD_ERR_INVALID_ARG;
+    }
+    const size_t need = workspace_need(shape, p, algo, p.dtt.on);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SSD_ERR_WORKSPACE;
+    const int64_t tokens = p.batch * p.seqlen;
+    if (!final_states || (tokens > 0 && (!x || !dt || !A || !B))) return SSD_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(dt, 4) || !aligned(A, 4) ||
+        !aligned(initial_states, 16) || !aligned(final_states, 16) || !aligned(cu_seqlens, 4))
+        return SSD_ERR_UNSUPPORTED;
+
+    p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = nullptr; p.D = nullptr;
+    p.init = initial_states; p.cu = cu_seqlens; p.y = nullptr; p.final_states = final_states;
+    p.states_only = true;
+    p.status = (int *)workspace;
+    p.ws = (char *)workspace + kStatusBytes;
+    p.ws_bytes = workspace_bytes - kStatusBytes;
+    p.stream = (cudaStream_t)stream;
+
+    if (cudaMemsetAsync(p.status, 0, sizeof(int), p.stream) != cudaSuccess) return SSD_ERR_CUDA;
+    if (p.cu && launch_validate_cu(p) != cudaSuccess) return SSD_ERR_CUDA;
+    if (tokens == 0 || p.batch == 0) {
+        if (p.nseq > 0) {
+            const size_t bytes = (size_t)p.nseq * p.H * p.P * p.N * sizeof(float);
+            cudaError_t e = initial_states
+                ? cudaMemcpyAsync(final_states, initial_states, bytes, cudaMemcpyDeviceToDevice, p.stream)
+                : cudaMemsetAsync(final_states, 0, bytes, p.stream);
+            if (e != cudaSuccess) return SSD_ERR_CUDA;
+        }
+        return SSD_OK;
+    }
+    return fused_launch(p) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
 SSD_API int ssd_check_device_status(const void *workspace, void *stream) {
     if (!workspace) return SSD_ERR_INVALID_ARG;
     int status = 0;

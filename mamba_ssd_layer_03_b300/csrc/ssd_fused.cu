@@ -129,6 +129,12 @@ struct FArgs {
     float *logdec;
     float *hstart;             // [grid][state]: folded start state of each split (main run)
     int chain;
+    // State-only runs (kPre) serve two purposes: the first run of a split
+    // call, which records each split's partial state and log-decay
+    // (records), and a state-only scan (states_only), which takes splits
+    // like a main run does and writes the final states.
+    int records;
+    int states_only;
 };
 
 // One block of a CTA's walk as the compute warps need it, written by the TMA
@@ -401,12 +407,14 @@ __device__ __noinline__ void mask_chunk_exact(uint32_t taddr, float cs0, float c
 
 // kDtTransform: the step-size transform is compiled in only where a call asks
 // for it, so the plain scan carries no trace of it.
-// kPre: the state-only first run of a few-lane workload.  Each CTA runs
-// its range from a zero state where a lane began in an earlier CTA, skips
-// everything that only y needs (C, C B^T, C H^T, the mask, M x, the epilogue)
-// and records, where its range splits a lane, that partial state and the log
-// of its decay.  The second run (kPre false, chain set) starts each split
-// lane from those records instead of waiting for the previous CTA.
+// kPre: a state-only run, which skips everything that only y needs (C,
+// C B^T, C H^T, the mask, M x, the epilogue).  As the first run of a
+// few-lane workload (records set), each CTA runs its range from a zero state
+// where a lane began in an earlier CTA and records, where its range splits a
+// lane, that partial state and the log of its decay; the second run (chain
+// set) starts each split lane from those records instead of waiting for the
+// previous CTA.  As a state-only scan (states_only set) it takes splits like
+// a main run and writes the final states.
 template <bool kDtTransform, bool kWide, bool kPre>
 __global__ void __launch_bounds__(kThreads, 1)
 k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
@@ -769,7 +777,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                         const float *src = nullptr;
                         const int n_row = kWide ? 128 * h + t : t;   // this thread's state row
                         if (flags & kFromSlot) {
-                            if (kPre) {
+                            if (kPre && a.records) {
                             } else if (a.chain) {
                                 // folded from the pre run's records between the runs
                                 src = a.hstart + (size_t)ticket * kStateFloats + hs * kP * NS;
@@ -1028,13 +1036,16 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 tc_fence_after();
                 float *dst = nullptr;
                 if (fin) {
-                    // the pre run leaves final states to the main run
-                    if (!kPre && a.final_states && hv)
+                    // the recording run leaves final states to the main run
+                    if ((!kPre || a.states_only) && a.final_states && hv)
                         dst = a.final_states + ((int64_t)dk.s * a.H + head) * kP * NS;
-                } else if (kPre || !a.chain) {
-                    // handoff (pre run: the record the main run folds)
+                } else if (kPre && a.records) {
+                    // the record the main run folds
                     dst = a.hslot + (size_t)ticket * kStateFloats + hs * kP * NS;
-                    if (kPre && t == 0 && (!kWide || h == 0)) a.logdec[2 * ticket + hs] = ldsum;
+                    if (t == 0 && (!kWide || h == 0)) a.logdec[2 * ticket + hs] = ldsum;
+                } else if (!a.chain) {
+                    // handoff to the next CTA
+                    dst = a.hslot + (size_t)ticket * kStateFloats + hs * kP * NS;
                 }
 #pragma unroll 1
                 for (int c16 = 0; c16 < kP / 16; ++c16) {
@@ -1323,8 +1334,11 @@ cudaError_t fused_launch(const Problem &p) {
     const uint64_t dx[4] = {(uint64_t)p.P, (uint64_t)p.H, L, b};
     const uint64_t dbc[4] = {(uint64_t)p.N, (uint64_t)p.G, L, b};
     const uint32_t box[4] = {64, 1, (uint32_t)kB, 1};
+    // a state-only scan reads no C and writes no y: its maps of them are
+    // never used and point at B and x
     if (!make_map4(&tmX, p.x, dx, box) || !make_map4(&tmB, p.B, dbc, box) ||
-        !make_map4(&tmC, p.C, dbc, box) || !make_map4(&tmY, p.y, dx, box))
+        !make_map4(&tmC, p.states_only ? p.B : p.C, dbc, box) ||
+        !make_map4(&tmY, p.states_only ? p.x : p.y, dx, box))
         return cudaErrorInvalidValue;
 
     if (a.varlen) {
@@ -1332,6 +1346,7 @@ cudaError_t fused_launch(const Problem &p) {
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
+    a.states_only = p.states_only ? 1 : 0;
     const bool wide = p.N == 256;
     const size_t smem = wide ? smem_bytes<true>() : smem_bytes<false>();
     using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, FArgs);
@@ -1347,6 +1362,7 @@ cudaError_t fused_launch(const Problem &p) {
         // pre run: the state records at every split; then the tickets start
         // again from zero for the main run
         Kern pre = pick(true);
+        a.records = 1;
         e = check_regs(pre);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(pre, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1365,8 +1381,10 @@ cudaError_t fused_launch(const Problem &p) {
         // the first), so that no memset separates the kernels
         a.ticket += 1;
         a.chain = 1;
+        a.records = 0;
     }
-    Kern kern = pick(false);
+    // a state-only scan ends with a state-only run in place of the main run
+    Kern kern = pick(p.states_only);
     e = check_regs(kern);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

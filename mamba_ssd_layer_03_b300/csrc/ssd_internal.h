@@ -29,6 +29,7 @@ struct Problem {
     char *ws = nullptr;     // workspace after the status block
     size_t ws_bytes = 0;
     cudaStream_t stream = nullptr;
+    bool states_only = false;  // fused path only: final states, no y (ssd_scan_states)
 };
 
 // Bytes reserved at the start of every workspace for the status word.

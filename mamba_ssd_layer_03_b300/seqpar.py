@@ -6,9 +6,10 @@ sequence parallelism scales the layer to longer sequences.  Every batch row
 group (one GPU per rank).  The state is the only quantity that crosses a cut,
 so the ranks exchange it once:
 
-1. each rank scans its shard from a zero state (``ssd_scan``), giving the
-   state S_r its shard leaves, and sums its shard's log-decay
-   logdec_r[s, h] = sum_t dt'_t A_h (``ssd_seqpar_logdec``);
+1. each rank scans its shard's states from a zero state (``ssd_scan_states``
+   where the fused kernel takes the shape: no y is computed; else
+   ``ssd_scan``), giving the state S_r its shard leaves, and sums its
+   shard's log-decay logdec_r[s, h] = sum_t dt'_t A_h (``ssd_seqpar_logdec``);
 2. the ranks all-gather (S_r, logdec_r): H P N + 1 fp32 values per
    (sequence, head) and rank, copied into local buffers;
 3. each rank folds the gathered carries of the ranks before it into its
@@ -18,16 +19,15 @@ so the ranks exchange it once:
 4. each rank re-scans its shard from H_in(r) (``ssd_scan`` with
    initial_states), which gives its part of y exactly as the unsharded scan.
 
-Step 1's y is not needed; the rank's y buffer holds it until step 4
-overwrites it, so the exchange allocates only the gathered carries.  The
-cost per rank is two scans of its shard, one log-decay pass, one fold and one
-all_gather of (H P N + H) x batch x world fp32.
+The cost per rank is one state-only scan and one full scan of its shard, one
+log-decay pass, one fold and one all_gather of (H P N + H) x batch x world
+fp32.
 
 ``ssd_scan_seqpar`` composes these steps through an ``ops`` object with the
-three device steps (``scan``, ``logdec``, ``fold``) and the collective
+device steps (``states``, ``scan``, ``logdec``, ``fold``) and the collective
 (``exchange``); the default, ``CudaOps``, calls the library's kernels through
 the C ABI and gathers on the tensors' device (NCCL).  Any other object with
-the same four methods can stand in, for example to check the composition and
+the same five methods can stand in, for example to check the composition and
 the collective on CPU ranks.
 """
 from __future__ import annotations
@@ -38,7 +38,8 @@ from typing import Optional
 import torch
 import torch.distributed as dist
 
-from . import (SsdError, _check, _ptr, load_library, make_dt_transform, make_shape, ssd_scan)
+from . import (SsdError, _check, _ptr, load_library, make_dt_transform, make_shape,
+               resolve_algo, ssd_scan, ssd_scan_states)
 
 
 def shard_logdec(dt: torch.Tensor, A: torch.Tensor, dt_bias: Optional[torch.Tensor] = None,
@@ -121,6 +122,15 @@ class CudaOps:
         return ssd_scan(x, dt, A, B, C, D, chunk_size, initial_states, None, final, self.algo,
                         out=out, **self.dt)
 
+    def states(self, x, dt, A, B, C, chunk_size):
+        """The shard's end state from a zero state: the state-only scan where
+        the fused kernel takes the shape, else a full scan's final states."""
+        b, L, H, P = x.shape
+        shape = make_shape(b, L, H, P, B.shape[3], B.shape[2], chunk_size, b, x.dtype, self.algo)
+        if resolve_algo(shape) == "tc":
+            return ssd_scan_states(x, dt, A, B, chunk_size, None, None, self.algo, **self.dt)
+        return self.scan(x, dt, A, B, C, None, chunk_size, None)[1]
+
     def logdec(self, dt, A):
         return shard_logdec(dt, A, **self.dt)
 
@@ -158,14 +168,13 @@ def ssd_scan_seqpar(x, dt, A, B, C, D=None, chunk_size: int = 256, initial_state
     """
     ops = ops if ops is not None else CudaOps()
     rank = dist.get_rank(group)
-    # 1. local carry from a zero state (its y is discarded: the buffer is
-    #    reused by the re-scan)
-    y, S = ops.scan(x, dt, A, B, C, None, chunk_size, None)
+    # 1. local carry from a zero state
+    S = ops.states(x, dt, A, B, C, chunk_size)
     ld = ops.logdec(dt, A)
     # 2. exchange
     S_all, ld_all = ops.exchange(S, ld, group)
     # 3. fold the shards before this one into the entry state
     entry, final = ops.fold(S_all, ld_all, rank, initial_states)
     # 4. the shard's output from its true entry state
-    y, _ = ops.scan(x, dt, A, B, C, D, chunk_size, entry, out=y, final=False)
+    y, _ = ops.scan(x, dt, A, B, C, D, chunk_size, entry, final=False)
     return y, final

@@ -300,3 +300,26 @@ def test_noalloc_wrapper_refuses_host_tensors():
     B = torch.zeros(1, 8, 1, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         ssd.ssd_scan_noalloc(x, torch.zeros(1, 8, 2), torch.zeros(2), B, B, None, 256)
+
+
+def test_scan_states_rejects_on_host():
+    """ssd_scan_states: shapes the fused kernel does not take, missing
+    outputs and short workspaces are refused before any device work."""
+    import torch
+    lib = ssd.load_library()
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced
+    ws = ctypes.c_void_p(1 << 24)
+
+    def call(shape, final=fake, wsb=1 << 30, x=fake):
+        return lib.ssd_scan_states(ctypes.byref(shape), x, fake, None, fake, fake, None, None,
+                                   final, ws, ctypes.c_size_t(wsb), None)
+
+    # (the fused kernel's shapes need the driver's tensor-map encoder, so the
+    # checks of those shapes run with the GPU tests)
+    assert lib.ssd_scan_states(None, fake, fake, None, fake, fake, None, None, fake, ws,
+                               ctypes.c_size_t(1 << 30), None) == 1
+    assert call(ssd.make_shape(2, 512, 4, 64, 128, 1, 256, 2, torch.float32, "auto")) == 2
+    assert call(ssd.make_shape(2, 512, 4, 32, 128, 1, 256, 2, torch.bfloat16, "auto")) == 2
+    assert call(ssd.make_shape(2, 512, 4, 64, 128, 1, 256, 2, torch.bfloat16, "tc2")) == 2
+    assert call(ssd.make_shape(2, 512, 4, 64, 128, 1, 256, 2, torch.bfloat16, "simt")) == 2
+    assert call(ssd.make_shape(2, 512, 4, 64, 128, 1, 7, 2, torch.bfloat16, "auto")) == 2

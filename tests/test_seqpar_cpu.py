@@ -38,6 +38,9 @@ class OracleOps:
         y, fin = oracle.recurrent(x, dt, A, B, C, D, initial_states)
         return torch.from_numpy(y), torch.from_numpy(fin)
 
+    def states(self, x, dt, A, B, C, chunk_size):
+        return self.scan(x, dt, A, B, C, None, chunk_size, None)[1]
+
     def logdec(self, dt, A):
         a = dt.to(torch.float64) * A.to(torch.float64)          # (b, L, H)
         return a.sum(dim=1)
