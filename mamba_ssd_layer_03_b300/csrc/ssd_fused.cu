@@ -12,7 +12,9 @@
 // with dstate 256 (wide lanes).  Its blocks are consecutive 128-token pieces
 // of the sequence.  All blocks of all lanes are numbered lane-major and every
 // CTA takes a contiguous range of that numbering (its "ticket" decides which),
-// so the load is balanced to within one block.  A CTA walks its blocks in
+// so the load is balanced to within one block.  (Split wide lanes number sets
+// of lanes of one B/C group instead, and a set of CTAs shares each range, one
+// lane apiece: see set_blocks.)  A CTA walks its blocks in
 // order and keeps the running state of its lane in TMEM.  When a lane is
 // split between two CTAs, the earlier CTA hands the state at the split point
 // to the later one through global memory; every CTA processes the lane it
@@ -112,6 +114,10 @@ struct FArgs {
     int H, G, hpg, npg, ptot;  // heads, groups, heads per group, lanes per group, lanes per sequence
     int hpl;                   // heads per lane (2 narrow, 1 wide)
     int nseq, varlen, nb_fixed, grid;
+    // CTAs per lane set: the qs CTAs with tickets qs v .. qs v + qs - 1
+    // take the same block range of qs lanes of one B/C group, one lane each
+    // (qs = 1: ranges of single lanes)
+    int qs;
     const float *dt, *A, *D, *init;
     const int32_t *cu;
     bf16 *y;
@@ -221,7 +227,21 @@ __device__ __forceinline__ Lane lane_info(const FArgs &a, int64_t l) {
     return n;
 }
 
-// Lane that holds global block g (0 <= g < total_blocks).
+// Lane sets: with qs > 1 (fixed-length sequences only) the ranges are cut
+// in the numbering of sets of qs lanes of one B/C group, lane-set-major; set
+// v is lanes qs v .. qs v + qs - 1, and a set's block b stands for block b
+// of each of its lanes.  The qs CTAs of a ticket set take the same range, one
+// lane of each set apiece, so they reach the same B and C tiles at about the
+// same time.  The kernel passes qs as a constant 1 where it never differs
+// (narrow lanes), which leaves their index arithmetic as it was.
+__device__ __forceinline__ int64_t set_blocks(const FArgs &a, int qs) { return total_blocks(a) / qs; }
+
+// First global block of lane set v (= lane v when qs = 1).
+__device__ __forceinline__ int64_t set_start(const FArgs &a, int64_t v) {
+    return a.varlen ? lane_info(a, v).start : v * a.nb_fixed;
+}
+
+// Lane set that holds set-numbered block g (0 <= g < set_blocks).
 __device__ __forceinline__ int64_t find_lane(const FArgs &a, int64_t g) {
     if (!a.varlen) return g / a.nb_fixed;
     int lo = 0, hi = a.nseq - 1;
@@ -235,11 +255,19 @@ __device__ __forceinline__ int64_t find_lane(const FArgs &a, int64_t g) {
     return (int64_t)lo * a.ptot + pair;
 }
 
-// The blocks of one CTA: range [g0, g1) of the global numbering, visited
-// lane by lane in the order last lane, middle lanes, first lane.
+// The blocks of one CTA: range [g0, g1) of the lane-set numbering, visited
+// lane by lane in the order last lane, middle lanes, first lane.  The
+// state-only runs of a split call leave out the segments whose state nobody
+// reads: the recording run needs only a segment that ends inside its lane
+// (the partial state the fold takes; at most one per CTA, its last lane),
+// and a state-only main run only the segments that end a lane (final
+// states).
+enum : int { kSegAll = 0, kSegSplit = 1, kSegFinal = 2 };
 struct Walk {
-    int64_t g0, g1, l0, l1, nl;
+    int64_t g0, g1, l0, l1, nl;   // l0, l1: lane sets
     int64_t k;      // segment index in visiting order
+    int qs, member; // CTAs per set; which lane of each set
+    int need;       // segments visited: kSegAll, kSegSplit, kSegFinal
     Lane ln;
     int b, b_begin, b_end;
     bool valid;
@@ -253,11 +281,14 @@ __device__ __forceinline__ int64_t seg_lane(const Walk &w, int64_t k) {
 
 __device__ __forceinline__ void walk_load_seg(const FArgs &a, Walk &w) {
     while (w.k < w.nl) {
-        w.ln = lane_info(a, seg_lane(w, w.k));
-        const int64_t lo = max64(w.g0, w.ln.start), hi = min64(w.g1, w.ln.start + w.ln.nb);
-        if (lo < hi) {
-            w.b_begin = (int)(lo - w.ln.start);
-            w.b_end = (int)(hi - w.ln.start);
+        const int64_t v = seg_lane(w, w.k);
+        w.ln = lane_info(a, v * w.qs + w.member);
+        const int64_t v0 = a.varlen ? w.ln.start : v * a.nb_fixed;   // set_start
+        const int64_t lo = max64(w.g0, v0), hi = min64(w.g1, v0 + w.ln.nb);
+        const bool fin = hi == v0 + w.ln.nb;
+        if (lo < hi && (w.need == kSegAll || (w.need == kSegFinal) == fin)) {
+            w.b_begin = (int)(lo - v0);
+            w.b_end = (int)(hi - v0);
             w.b = w.b_begin;
             w.valid = true;
             return;
@@ -267,16 +298,24 @@ __device__ __forceinline__ void walk_load_seg(const FArgs &a, Walk &w) {
     w.valid = false;
 }
 
-// Number of blocks in the range of CTA `ticket`.
-__device__ __forceinline__ int cta_blocks(const FArgs &a, int ticket) {
-    const int64_t T = total_blocks(a);
-    return (int)((int64_t)(ticket + 1) * T / a.grid - (int64_t)ticket * T / a.grid);
+// First block (lane-set numbering) of the range of ticket set u.
+__device__ __forceinline__ int64_t range_begin(const FArgs &a, int64_t u, int qs) {
+    return u * set_blocks(a, qs) / (a.grid / qs);
 }
 
-__device__ __forceinline__ void walk_init(const FArgs &a, Walk &w, int ticket) {
-    const int64_t T = total_blocks(a);
-    w.g0 = (int64_t)ticket * T / a.grid;
-    w.g1 = (int64_t)(ticket + 1) * T / a.grid;
+// Number of blocks in the range of CTA `ticket`.
+__device__ __forceinline__ int cta_blocks(const FArgs &a, int ticket, int qs) {
+    const int u = ticket / qs;
+    return (int)(range_begin(a, u + 1, qs) - range_begin(a, u, qs));
+}
+
+__device__ __forceinline__ void walk_init(const FArgs &a, Walk &w, int ticket, int qs, int need) {
+    const int u = ticket / qs;
+    w.qs = qs;
+    w.need = need;
+    w.member = ticket % qs;
+    w.g0 = range_begin(a, u, qs);
+    w.g1 = range_begin(a, u + 1, qs);
     w.valid = false;
     if (w.g0 >= w.g1) return;
     w.l0 = find_lane(a, w.g0);
@@ -290,6 +329,20 @@ __device__ __forceinline__ void walk_next(const FArgs &a, Walk &w) {
     if (++w.b < w.b_end) return;
     ++w.k;
     walk_load_seg(a, w);
+}
+
+// Blocks a run visits in the range of CTA `ticket`.
+__device__ __forceinline__ int run_blocks(const FArgs &a, int ticket, int qs, int need) {
+    if (need == kSegAll) return cta_blocks(a, ticket, qs);
+    Walk w;
+    walk_init(a, w, ticket, qs, need);
+    int n = 0;
+    while (w.valid) {
+        n += w.b_end - w.b_begin;
+        ++w.k;
+        walk_load_seg(a, w);
+    }
+    return n;
 }
 
 // ----------------------------------------------------------------------------
@@ -459,6 +512,10 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     const uint32_t tbase = sm->tmem;
     const uint32_t R_cb = tbase, R_H = tbase + 128;
     const int ticket = sm->ticket;
+    const int qs = kWide ? a.qs : 1;   // CTAs per lane set (only split wide lanes use sets)
+    const int need = !kPre ? kSegAll
+                   : a.records ? kSegSplit
+                   : (a.states_only && a.chain) ? kSegFinal : kSegAll;
     // packed sequences: every role reads the lane table that
     // k_fused_varlen_setup, launched just before, writes
     if (a.varlen) grid_dep_wait();
@@ -472,7 +529,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         // ------------------------------------------------------------ TMA
         if (lane == 0 && run) {
             Walk w;
-            walk_init(a, w, ticket);
+            walk_init(a, w, ticket, qs, need);
             uint32_t k = 0;
             for (; w.valid; walk_next(a, w), ++k) {
                 const int tok = (int)(w.ln.t0 + (int64_t)w.b * kB);
@@ -557,7 +614,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             const uint32_t id_mx = idesc_bf16_f32(128, 64, 0, 1);
             const uint32_t sc = smem_u32(sC), sbb = smem_u32(sB), sxw = smem_u32(sXw),
                            sh = smem_u32(sH), sx = smem_u32(sX);
-            const uint32_t nblk = (uint32_t)cta_blocks(a, ticket);
+            const uint32_t nblk = (uint32_t)run_blocks(a, ticket, qs, need);
             for (uint32_t k = 0; k < nblk; ++k) {
                 const int slot = k & 1;
                 const uint32_t R_acc = tbase + 256 + Gm::ACC * slot;
@@ -650,7 +707,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         if (!kPre && run) {
             const int t = tid & 127;
             const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-            const uint32_t nblk = (uint32_t)cta_blocks(a, ticket);
+            const uint32_t nblk = (uint32_t)run_blocks(a, ticket, qs, need);
             for (uint32_t k = 0; k < nblk; ++k) {
                 const int slot = k & 1;
                 fwait(&sm->desc_full[k % kDescRing], (k / kDescRing) & 1, a.status);
@@ -742,7 +799,7 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         };
         bool have_next = false;
         float ldsum = 0.f;         // pre run: sum of cs_last over the lane's blocks here
-        const uint32_t nblk = (uint32_t)cta_blocks(a, ticket);
+        const uint32_t nblk = (uint32_t)run_blocks(a, ticket, qs, need);
         // the main run of a split call starts splits from the fold's states:
         // wait for the fold (and with it the pre run) to complete
         grid_dep_wait();
@@ -782,8 +839,9 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                                 // folded from the pre run's records between the runs
                                 src = a.hstart + (size_t)ticket * kStateFloats + hs * kP * NS;
                             } else {
-                                wait_flag(a.hflag + (ticket - 1), a.status);
-                                src = a.hslot + (size_t)(ticket - 1) * kStateFloats + hs * kP * NS;
+                                // the previous range of this lane: ticket - qs
+                                wait_flag(a.hflag + (ticket - qs), a.status);
+                                src = a.hslot + (size_t)(ticket - qs) * kStateFloats + hs * kP * NS;
                             }
                         } else if (a.init && hv) {
                             src = a.init + ((int64_t)dk.s * a.H + head) * kP * NS;
@@ -1076,9 +1134,11 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 }
 
 // Between the two runs of a few-lane workload: for every CTA whose range
-// begins inside a lane, its start state.  Ticket u0's range holds the lane's
-// first block, so its pre-run record is the whole state up to its range end;
-// every later ticket u before this one adds H <- exp(logdec_u) H + S_u.
+// begins inside a lane, its start state.  The earlier ranges of the lane are
+// those of tickets ticket - qs, ticket - 2 qs, ... (one per ticket set).
+// Ticket u0's range holds the lane's first block, so its pre-run record is
+// the whole state up to its range end; every later ticket u before this one
+// adds H <- exp(logdec_u) H + S_u.
 // Grid: y over the tickets, x over 1024-value slices of the state, one float4
 // per thread, so that every thread has its whole chain of loads in flight
 // (a CTA per ticket looping over the state ran latency-bound).
@@ -1090,17 +1150,20 @@ __global__ void __launch_bounds__(kFoldThreads) k_fused_chain_fold(FArgs a, int 
     grid_dep_wait();   // the pre run's records
     if (status_bad(a.status)) return;
     const int ticket = blockIdx.y;
-    const int64_t T = total_blocks(a);
-    const int64_t g0 = (int64_t)ticket * T / a.grid;
-    if (ticket == 0 || g0 >= T) return;
-    const Lane ln = lane_info(a, find_lane(a, g0));
-    if (ln.start >= g0) return;      // the range begins at a lane start
-    int u0 = ticket - 1;
-    while (u0 > 0 && (int64_t)u0 * T / a.grid > ln.start) --u0;
+    const int qs = a.qs, us = ticket / qs, m = ticket % qs;   // ticket set, lane of each set
+    const int vg = a.grid / qs;
+    const int64_t TS = set_blocks(a, qs);
+    const int64_t g0 = (int64_t)us * TS / vg;                 // range_begin
+    if (us == 0 || g0 >= TS) return;
+    const int64_t v0 = set_start(a, find_lane(a, g0));
+    if (v0 >= g0) return;      // the range begins at a lane start
+    // the last ticket set whose range begins at or before the lane start:
+    // u TS / vg <= v0 (rounded down) exactly when u <= ((v0 + 1) vg - 1) / TS
+    const int u0 = (int)min64(us - 1, ((v0 + 1) * vg - 1) / TS);
     const int e = 4 * (blockIdx.x * kFoldThreads + threadIdx.x);
     const int hs = e / (kP * NS);
-    float4 hv = __ldcg(reinterpret_cast<const float4 *>(a.hslot + (size_t)u0 * kStateFloats + e));
-    for (int u = u0 + 1; u < ticket; ++u) {
+    float4 hv = __ldcg(reinterpret_cast<const float4 *>(a.hslot + (size_t)(u0 * qs + m) * kStateFloats + e));
+    for (int u = (u0 + 1) * qs + m; u < ticket; u += qs) {
         const float d = __expf(__ldcg(a.logdec + 2 * u + hs));
         const float4 s = __ldcg(reinterpret_cast<const float4 *>(a.hslot + (size_t)u * kStateFloats + e));
         hv.x = fmaf(d, hv.x, s.x);
@@ -1218,6 +1281,7 @@ struct FLayout {
     size_t hdr, slots, logdec, hstart, seqblk, total;
     int grid;
     bool chain;   // few lanes: split them between CTAs, pre run + main run
+    int qs;       // CTAs per lane set
 };
 
 // Heads per lane: two of a group with dstate 128, one with dstate 256.
@@ -1234,6 +1298,7 @@ int64_t lanes_per_seq(const Problem &p) {
 // per SM, so its size does not depend on cu_seqlens.
 FLayout fused_layout(const Problem &p) {
     FLayout w{};
+    w.qs = 1;
     const int64_t ptot = lanes_per_seq(p);
     const int64_t sms = sm_count();
     const int64_t nb = (p.seqlen + kB - 1) / kB;
@@ -1245,6 +1310,21 @@ FLayout fused_layout(const Problem &p) {
         // between CTAs, which start from the pre run's records.
         grid = min64(sms, (int64_t)p.nseq * ptot * nb / kChainMinCtaBlocks);
         w.chain = true;
+        // Wide lanes hold one head each, so the lanes of one B/C group read
+        // the same B and C tiles, and a group's tiles over the whole
+        // sequence outgrow L2 (64 KB per block).  Split ranges cut lane by
+        // lane reach those tiles tens of blocks apart and re-read them from
+        // DRAM; sets of CTAs that take the same range of a group's lanes
+        // reach them together.  The set is the largest divisor of the lanes
+        // per group up to 8, and the grid a multiple of it.
+        const int npg = (int)(ptot / p.G);
+        if (p.N == 256 && npg > 1) {
+            int q = 1;
+            for (int d = 2; d <= 8; ++d)
+                if (npg % d == 0 && grid >= d) q = d;
+            w.qs = q;
+            grid = grid / q * q;
+        }
     } else {
         grid = min64(sms, (int64_t)p.nseq * ptot);
     }
@@ -1314,6 +1394,7 @@ cudaError_t fused_launch(const Problem &p) {
     a.varlen = p.cu != nullptr;
     a.nb_fixed = (int)((p.seqlen + kB - 1) / kB);
     a.grid = w.grid;
+    a.qs = w.qs;
     a.dt = p.dt; a.A = p.A; a.D = p.D; a.init = p.init; a.cu = p.cu;
     a.dtt = p.dtt;
     a.y = (bf16 *)p.y;

@@ -304,7 +304,12 @@ def test_wide_lanes_packed_sequences(segs):
     (1, dict(seed=62, batch=1, seqlen=6000, nheads=6, init_states=True)),    # 3 lanes, ragged tail
     (3, dict(seed=63, batch=1, seqlen=8192, nheads=8, init_states=True)),    # wide lanes
     (1, dict(seed=64, batch=2, seqlen=2048, nheads=24, init_states=True)),   # 4 blocks per CTA, lane-aligned
-], ids=["narrow", "straddle", "wide", "four_blocks"])
+    # wide lanes, several heads per B/C group (8 groups): CTAs in sets of 4, 3
+    # and 6 take the same range of a group's lanes, one lane each
+    (3, dict(seed=65, batch=1, seqlen=4096, nheads=32, init_states=True)),
+    (3, dict(seed=66, batch=2, seqlen=2500, nheads=24, init_states=True)),
+    (3, dict(seed=67, batch=1, seqlen=3000, nheads=48, init_states=False)),
+], ids=["narrow", "straddle", "wide", "four_blocks", "wide_sets4", "wide_sets3_ragged", "wide_sets6"])
 def test_split_lanes_two_runs(wi, kw):
     inp = ssd_synth.make_inputs(W[wi], **kw)
     _compare_full(inp, "tc")

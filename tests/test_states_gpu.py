@@ -24,6 +24,8 @@ CASES = [
     ("wide_grouped", 3, dict(batch=1, seqlen=900, nheads=8, init_states=True)),
     ("split_lanes", 1, dict(batch=1, seqlen=8192, nheads=2, init_states=True)),
     ("split_lanes_wide", 3, dict(batch=1, seqlen=8192, nheads=8, init_states=True)),
+    # four heads per B/C group: CTAs in sets of 4 share each range
+    ("split_lanes_wide_sets", 3, dict(batch=1, seqlen=4096, nheads=32, init_states=True)),
     ("varlen", 4, dict(seqlen=5000, nheads=4)),
 ]
 
