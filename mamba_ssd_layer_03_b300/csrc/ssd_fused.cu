@@ -467,7 +467,8 @@ __device__ __noinline__ void mask_chunk_exact(uint32_t taddr, float cs0, float c
 // lane, that partial state and the log of its decay; the second run (chain
 // set) starts each split lane from those records instead of waiting for the
 // previous CTA.  As a state-only scan (states_only set) it takes splits like
-// a main run and writes the final states.
+// a main run and writes the final states.  Either way it visits only the
+// segments whose state is read (see Walk).
 template <bool kDtTransform, bool kWide, bool kPre>
 __global__ void __launch_bounds__(kThreads, 1)
 k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
@@ -1060,15 +1061,19 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     // acc_h *= exp(cs_h[i]): narrow, head h's 64 columns; wide,
                     // columns [32 h, 32 h + 32) of the one head
                     const float e = __expf(h == 0 || kWide ? cs0 : cs1);
-#pragma unroll 1
-                    for (int half = 0; half < (kWide ? 1 : 2); ++half) {
-                        const uint32_t col = kWide ? 32 * h : 64 * h + 32 * half;
-                        uint32_t v[32];
-                        tmem_ld32(R_acc + lane_off + col, v);
+                    {
+                        // both halves' loads in flight before one wait
+                        uint32_t v[2][32];
+#pragma unroll
+                        for (int half = 0; half < (kWide ? 1 : 2); ++half)
+                            tmem_ld32(R_acc + lane_off + (kWide ? 32 * h : 64 * h + 32 * half), v[half]);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int q = 0; q < 32; q += 2) mul2(v[q], v[q + 1], e, e);
-                        tmem_st32(R_acc + lane_off + col, v);
+                        for (int half = 0; half < (kWide ? 1 : 2); ++half) {
+#pragma unroll
+                            for (int q = 0; q < 32; q += 2) mul2(v[half][q], v[half][q + 1], e, e);
+                            tmem_st32(R_acc + lane_off + (kWide ? 32 * h : 64 * h + 32 * half), v[half]);
+                        }
                     }
                     tmem_st_wait();
                 }
