@@ -762,8 +762,8 @@ def launches_per_step(algo, inp, sms=148):
     varlen = inp["cu_seqlens"] is not None
     if algo == "simt":
         return 4 + (2 if varlen else 0)
-    if algo == "tc":       # fused kernel (+ cu_seqlens check and set-up; + pre run and fold)
-        return 1 + (2 if varlen else 0) + (2 if fused_splits_lanes(inp, sms) else 0)
+    if algo == "tc":       # fused kernel (+ cu_seqlens check and set-up; + the pre run of split lanes)
+        return 1 + (2 if varlen else 0) + (1 if fused_splits_lanes(inp, sms) else 0)
     return 2
 
 

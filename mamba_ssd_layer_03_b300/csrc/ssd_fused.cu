@@ -22,9 +22,9 @@
 // waits.  With few long lanes (at most half as many as SMs) every lane is
 // split several ways, and waiting would chain the CTAs of a lane.  Such a
 // call runs the kernel twice: a state-only first run records each CTA's
-// partial state and decay where its range splits a lane,
-// k_fused_chain_fold passes the state across the splits, and the second
-// run starts every split from its folded state.
+// partial state and decay where its range splits a lane, and the second run
+// starts every split from those records, folded by the state-passing
+// recurrence at the split's start.
 //
 // Per block (tokens i, j in [0, 128), heads h of the lane, state H_h[p][n]
 // at the block start, cs_h = within-block cumulative sum of dt*A_h):
@@ -133,7 +133,7 @@ struct FArgs {
     // lane it hands off, [grid][2]; and the main run's flag to fold the state
     // at a split from those records instead of waiting for a handoff.
     float *logdec;
-    float *hstart;             // [grid][state]: folded start state of each split (main run)
+    float *hstart;             // unused (null): the kChain main run folds the records itself
     int chain;
     // State-only runs (kPre) serve two purposes: the first run of a split
     // call, which records each split's partial state and log-decay
@@ -259,7 +259,7 @@ __device__ __forceinline__ int64_t find_lane(const FArgs &a, int64_t g) {
 // lane by lane in the order last lane, middle lanes, first lane.  The
 // state-only runs of a split call leave out the segments whose state nobody
 // reads: the recording run needs only a segment that ends inside its lane
-// (the partial state the fold takes; at most one per CTA, its last lane),
+// (the partial state the main run folds; at most one per CTA, its last lane),
 // and a state-only main run only the segments that end a lane (final
 // states).
 enum : int { kSegAll = 0, kSegSplit = 1, kSegFinal = 2 };
@@ -469,7 +469,11 @@ __device__ __noinline__ void mask_chunk_exact(uint32_t taddr, float cs0, float c
 // previous CTA.  As a state-only scan (states_only set) it takes splits like
 // a main run and writes the final states.  Either way it visits only the
 // segments whose state is read (see Walk).
-template <bool kDtTransform, bool kWide, bool kPre>
+// kChain: the main run of a split call.  A CTA whose range begins inside a
+// lane folds the pre run's records into its start state itself.  (Only the
+// instances that split calls launch hold that code: the single-run kernel's
+// loop is sensitive to its code size and layout.)
+template <bool kDtTransform, bool kWide, bool kPre, bool kChain>
 __global__ void __launch_bounds__(kThreads, 1)
 k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmY,
@@ -801,8 +805,8 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         bool have_next = false;
         float ldsum = 0.f;         // pre run: sum of cs_last over the lane's blocks here
         const uint32_t nblk = (uint32_t)run_blocks(a, ticket, qs, need);
-        // the main run of a split call starts splits from the fold's states:
-        // wait for the fold (and with it the pre run) to complete
+        // the main run of a split call starts splits from the pre run's
+        // records: wait for the pre run to complete
         grid_dep_wait();
 
         for (uint32_t k = 0;; ++k) {
@@ -834,11 +838,32 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                         // handoff.
                         const float *src = nullptr;
                         const int n_row = kWide ? 128 * h + t : t;   // this thread's state row
+                        int uf = 0, ue = 0;   // later records to fold in: tickets uf, uf + qs, ... < ue
                         if (flags & kFromSlot) {
                             if (kPre && a.records) {
                             } else if (a.chain) {
-                                // folded from the pre run's records between the runs
-                                src = a.hstart + (size_t)ticket * kStateFloats + hs * kP * NS;
+                                if constexpr (kPre || kChain) {
+                                    // The state-passing recurrence across the splits,
+                                    // over the pre run's records (complete: the compute
+                                    // warps waited for the pre run).  The lane's earlier
+                                    // ranges are those of tickets qs apart; ticket set
+                                    // u0's range holds the lane's first block, so its
+                                    // record is the state up to its end, and each later
+                                    // range's adds H <- exp(logdec_u) H + S_u.
+                                    const int us = ticket / qs, mb = ticket % qs, vg = a.grid / qs;
+                                    const int64_t TS = set_blocks(a, qs);
+                                    const int64_t v0 = set_start(a, find_lane(a, (int64_t)us * TS / vg));
+                                    // the last ticket set whose range begins at or before
+                                    // the lane start: u TS / vg <= v0 (rounded down)
+                                    // exactly when u <= ((v0 + 1) vg - 1) / TS
+                                    const int u0 = (int)min64(us - 1, ((v0 + 1) * vg - 1) / TS);
+                                    src = a.hslot + (size_t)(u0 * qs + mb) * kStateFloats + hs * kP * NS;
+                                    uf = (u0 + 1) * qs + mb;
+                                    ue = ticket;
+                                } else {
+                                    // not taken: split calls launch the kChain instance
+                                    src = a.hstart + (size_t)ticket * kStateFloats + hs * kP * NS;
+                                }
                             } else {
                                 // the previous range of this lane: ticket - qs
                                 wait_flag(a.hflag + (ticket - qs), a.status);
@@ -856,6 +881,17 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 #pragma unroll
                                 for (int q = 0; q < 16; ++q)
                                     r[q] = __float_as_uint(__ldcg(src + (c16 * 16 + q) * NS + n_row));
+                                if constexpr (kPre || kChain) {
+#pragma unroll 1
+                                    for (int u = uf; u < ue; u += qs) {
+                                        const float d = __expf(__ldcg(a.logdec + 2 * u + hs));
+                                        const float *su = a.hslot + (size_t)u * kStateFloats + hs * kP * NS;
+#pragma unroll
+                                        for (int q = 0; q < 16; ++q)
+                                            r[q] = __float_as_uint(fmaf(d, __uint_as_float(r[q]),
+                                                                        __ldcg(su + (c16 * 16 + q) * NS + n_row)));
+                                    }
+                                }
                                 tmem_st16(R_H + lane_off + h * 64 + c16 * 16, r);
                             }
                         } else {
@@ -1138,47 +1174,6 @@ k_ssd_fused(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
-// Between the two runs of a few-lane workload: for every CTA whose range
-// begins inside a lane, its start state.  The earlier ranges of the lane are
-// those of tickets ticket - qs, ticket - 2 qs, ... (one per ticket set).
-// Ticket u0's range holds the lane's first block, so its pre-run record is
-// the whole state up to its range end; every later ticket u before this one
-// adds H <- exp(logdec_u) H + S_u.
-// Grid: y over the tickets, x over 1024-value slices of the state, one float4
-// per thread, so that every thread has its whole chain of loads in flight
-// (a CTA per ticket looping over the state ran latency-bound).
-constexpr int kFoldThreads = 256;
-constexpr int kFoldSlices = kStateFloats / (4 * kFoldThreads);
-static_assert(kStateFloats % (4 * kFoldThreads) == 0, "fold slices");
-__global__ void __launch_bounds__(kFoldThreads) k_fused_chain_fold(FArgs a, int NS) {
-    if (threadIdx.x == 0) grid_dep_launch();
-    grid_dep_wait();   // the pre run's records
-    if (status_bad(a.status)) return;
-    const int ticket = blockIdx.y;
-    const int qs = a.qs, us = ticket / qs, m = ticket % qs;   // ticket set, lane of each set
-    const int vg = a.grid / qs;
-    const int64_t TS = set_blocks(a, qs);
-    const int64_t g0 = (int64_t)us * TS / vg;                 // range_begin
-    if (us == 0 || g0 >= TS) return;
-    const int64_t v0 = set_start(a, find_lane(a, g0));
-    if (v0 >= g0) return;      // the range begins at a lane start
-    // the last ticket set whose range begins at or before the lane start:
-    // u TS / vg <= v0 (rounded down) exactly when u <= ((v0 + 1) vg - 1) / TS
-    const int u0 = (int)min64(us - 1, ((v0 + 1) * vg - 1) / TS);
-    const int e = 4 * (blockIdx.x * kFoldThreads + threadIdx.x);
-    const int hs = e / (kP * NS);
-    float4 hv = __ldcg(reinterpret_cast<const float4 *>(a.hslot + (size_t)(u0 * qs + m) * kStateFloats + e));
-    for (int u = (u0 + 1) * qs + m; u < ticket; u += qs) {
-        const float d = __expf(__ldcg(a.logdec + 2 * u + hs));
-        const float4 s = __ldcg(reinterpret_cast<const float4 *>(a.hslot + (size_t)u * kStateFloats + e));
-        hv.x = fmaf(d, hv.x, s.x);
-        hv.y = fmaf(d, hv.y, s.y);
-        hv.z = fmaf(d, hv.z, s.z);
-        hv.w = fmaf(d, hv.w, s.w);
-    }
-    *reinterpret_cast<float4 *>(a.hstart + (size_t)ticket * kStateFloats + e) = hv;
-}
-
 // Varlen set-up: blocks per sequence (exclusive prefix) and the final states
 // of empty sequences (their initial states).  One CTA.
 __global__ void k_fused_varlen_setup(FArgs a, int P, int N) {
@@ -1283,7 +1278,7 @@ constexpr int64_t kChainMinLaneBlocks = 16;   // blocks per lane
 constexpr int64_t kChainMinCtaBlocks = 4;     // blocks per CTA
 
 struct FLayout {
-    size_t hdr, slots, logdec, hstart, seqblk, total;
+    size_t hdr, slots, logdec, seqblk, total;
     int grid;
     bool chain;   // few lanes: split them between CTAs, pre run + main run
     int qs;       // CTAs per lane set
@@ -1341,8 +1336,6 @@ FLayout fused_layout(const Problem &p) {
     off = align_up(off + (size_t)sms * kStateFloats * sizeof(float), 256);
     w.logdec = off;
     off = align_up(off + (size_t)sms * 2 * sizeof(float), 256);
-    w.hstart = off;
-    off = align_up(off + (size_t)sms * kStateFloats * sizeof(float), 256);
     w.seqblk = off;
     off = align_up(off + (size_t)(p.nseq + 1) * sizeof(int), 256);
     w.total = off;
@@ -1409,7 +1402,7 @@ cudaError_t fused_launch(const Problem &p) {
     a.hflag = (int *)(p.ws + w.hdr + 256);
     a.hslot = (float *)(p.ws + w.slots);
     a.logdec = (float *)(p.ws + w.logdec);
-    a.hstart = (float *)(p.ws + w.hstart);
+    a.hstart = nullptr;   // split calls fold their start states in the main run
     a.seqblk = (const int *)(p.ws + w.seqblk);
 
     cudaError_t e = cudaMemsetAsync(p.ws + w.hdr, 0, w.slots - w.hdr, p.stream);
@@ -1436,18 +1429,20 @@ cudaError_t fused_launch(const Problem &p) {
     const bool wide = p.N == 256;
     const size_t smem = wide ? smem_bytes<true>() : smem_bytes<false>();
     using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, FArgs);
-    auto pick = [&](bool pre) -> Kern {
+    auto pick = [&](bool pre, bool chain) -> Kern {
         if (wide) {
-            if (pre) return a.dtt.on ? k_ssd_fused<true, true, true> : k_ssd_fused<false, true, true>;
-            return a.dtt.on ? k_ssd_fused<true, true, false> : k_ssd_fused<false, true, false>;
+            if (pre) return a.dtt.on ? k_ssd_fused<true, true, true, false> : k_ssd_fused<false, true, true, false>;
+            if (chain) return a.dtt.on ? k_ssd_fused<true, true, false, true> : k_ssd_fused<false, true, false, true>;
+            return a.dtt.on ? k_ssd_fused<true, true, false, false> : k_ssd_fused<false, true, false, false>;
         }
-        if (pre) return a.dtt.on ? k_ssd_fused<true, false, true> : k_ssd_fused<false, false, true>;
-        return a.dtt.on ? k_ssd_fused<true, false, false> : k_ssd_fused<false, false, false>;
+        if (pre) return a.dtt.on ? k_ssd_fused<true, false, true, false> : k_ssd_fused<false, false, true, false>;
+        if (chain) return a.dtt.on ? k_ssd_fused<true, false, false, true> : k_ssd_fused<false, false, false, true>;
+        return a.dtt.on ? k_ssd_fused<true, false, false, false> : k_ssd_fused<false, false, false, false>;
     };
     if (w.chain) {
         // pre run: the state records at every split; then the tickets start
         // again from zero for the main run
-        Kern pre = pick(true);
+        Kern pre = pick(true, false);
         a.records = 1;
         e = check_regs(pre);
         if (e != cudaSuccess) return e;
@@ -1460,9 +1455,6 @@ cudaError_t fused_launch(const Problem &p) {
             e = cudaGetLastError();
         }
         if (e != cudaSuccess) return e;
-        e = launch_dependent(k_fused_chain_fold, dim3(kFoldSlices, w.grid), kFoldThreads, 0, p.stream,
-                             a, p.N);
-        if (e != cudaSuccess) return e;
         // the main run draws its tickets from a second counter (zeroed with
         // the first), so that no memset separates the kernels
         a.ticket += 1;
@@ -1470,7 +1462,7 @@ cudaError_t fused_launch(const Problem &p) {
         a.records = 0;
     }
     // a state-only scan ends with a state-only run in place of the main run
-    Kern kern = pick(p.states_only);
+    Kern kern = pick(p.states_only, w.chain);
     e = check_regs(kern);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
