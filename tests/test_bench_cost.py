@@ -1,7 +1,8 @@
 """The bench's roofline arithmetic, pinned to figures computed independently
 from the workload shapes: the byte and FLOP counts of the 2.7B-shaped and
 large-state layers (x, y, B, C, dt once each, plus the states; causal and
-dense FLOP counts of the block decomposition)."""
+dense FLOP counts of the block decomposition), the fused kernel's split rule,
+and the kernels one call launches (the gpu_launches figure)."""
 import pytest
 
 import bench
@@ -38,3 +39,19 @@ def test_fused_split_rule_on_the_workloads():
     assert bench.fused_splits_lanes(dict(_inp(2, 16384, 32, 64, 256, 8), cu_seqlens=None), 148)
     assert bench.fused_splits_lanes(dict(_inp(2, 2048, 24, 64, 128, 1), cu_seqlens=None), 148)
     assert not bench.fused_splits_lanes(dict(_inp(2, 1024, 24, 64, 128, 1), cu_seqlens=None), 148)
+
+
+def test_kernels_per_call_on_the_workloads():
+    # the gpu_launches claim: one fused launch; a split call adds its
+    # state-only pre run; packed sequences add the cu_seqlens check and the
+    # lane-table set-up; the SIMT path runs k1-k4 (+ the check and k5 with
+    # packing); the two-pass path its two kernels
+    one = dict(_inp(4, 8192, 80, 64, 128, 1), cu_seqlens=None)
+    split = dict(_inp(2, 16384, 32, 64, 256, 8), cu_seqlens=None)
+    packed = dict(_inp(1, 32768, 64, 64, 128, 1), cu_seqlens=object())
+    assert bench.launches_per_step("tc", one) == 1
+    assert bench.launches_per_step("tc", split) == 2
+    assert bench.launches_per_step("tc", packed) == 3
+    assert bench.launches_per_step("simt", one) == 4
+    assert bench.launches_per_step("simt", packed) == 6
+    assert bench.launches_per_step("tc2", one) == 2
